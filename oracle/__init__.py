@@ -1,0 +1,90 @@
+"""The oracle: a plain single-threaded CPU labeller (breadth-first flood fill).
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+benchmark's CPU-baseline leg may import this package.  It shares no code with
+the CUDA library and the CUDA library never calls it.
+
+What it computes (the plain definition; see ``ccl_oracle.c`` for citations):
+two pixels share a label exactly when a path of 4- or 8-neighbours of exactly
+equal value joins them ("every-colour", ch. 01-02); regions are numbered
+1..n in the raster order of their first pixel ("every-colour", ch. 04 and
+ch. 11); in binary mode value 0 is background and keeps label 0
+("every-colour", ch. 08 switch 4; bendabir.com, "The basic approach").
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "ccl_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB = os.path.join(_BUILD, "libccl_oracle.so")
+
+MODE_ALL = 0
+MODE_BINARY = 1
+
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with the host C compiler; returns the .so path."""
+    os.makedirs(_BUILD, exist_ok=True)
+    if (not force and os.path.exists(_LIB)
+            and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)):
+        return _LIB
+    tmp = _LIB + ".tmp%d" % os.getpid()
+    subprocess.check_call(["gcc", "-O2", "-std=c99", "-shared", "-fPIC",
+                           "-o", tmp, _SRC])
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            lib.oracle_label.restype = ctypes.c_int
+            lib.oracle_label.argtypes = [
+                ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                ctypes.c_void_p, ctypes.c_void_p]
+            _lib = lib
+    return _lib
+
+
+def label(img: np.ndarray, connectivity: int = 8, mode: int = MODE_ALL):
+    """Label a [B,]H,W image array (uint8 or uint32 pixels, or a trailing
+    byte axis for wider pixels).
+
+    Returns ``(labels int32 same leading shape, n_regions int32[B])``; for a
+    2-D input the batch axis is dropped from both.
+    """
+    a = np.ascontiguousarray(img)
+    squeeze = False
+    if a.dtype == np.uint8 and a.ndim == 4:      # [B,H,W,pixel_bytes]
+        B, H, W, pb = a.shape
+    elif a.ndim == 3:
+        B, H, W = a.shape
+        pb = a.dtype.itemsize
+    elif a.ndim == 2:
+        H, W = a.shape
+        B, pb = 1, a.dtype.itemsize
+        squeeze = True
+    else:
+        raise ValueError("expected a [B,]H,W array")
+    labels = np.empty((B, H, W), dtype=np.int32)
+    n = np.empty((B,), dtype=np.int32)
+    rc = _load().oracle_label(a.ctypes.data, B, H, W, pb, connectivity, mode,
+                              labels.ctypes.data, n.ctypes.data)
+    if rc != 0:
+        raise RuntimeError("oracle_label failed with status %d" % rc)
+    if squeeze:
+        return labels[0], n[0]
+    return labels, n

@@ -1,0 +1,133 @@
+/*
+ * ccl_oracle.c -- the oracle: plain, slow, single-threaded CPU labelling.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may include, link
+ * or call this file; it shares no code with the CUDA library.  Only the test
+ * suite, the smoke check and the benchmark's CPU-baseline leg use it.
+ *
+ * What it computes is the plain definition of the result, not the GPU method:
+ *
+ *   "every-colour" (blogs.fablnx.com), ch. 01 "The job" and ch. 02 "Regions":
+ *     two pixels share a number exactly when one can walk from one to the
+ *     other, one neighbour at a time, without changing colour; anti-aliased
+ *     shades are colours of their own; a pixel has eight neighbours (or four,
+ *     "About Connected Components Labeling on GPU", bendabir.com, Prologue).
+ *   "every-colour", ch. 04 "Point at a leader" and ch. 11 "How we know it is
+ *     right": a region's leader is its first pixel in reading order, and the
+ *     regions are numbered 1, 2, 3 ... in the reading order of their leaders.
+ *   "every-colour", ch. 08 switch 4 "Ignore the paper": pixels of the ignored
+ *     value get label 0 and join nothing.  Binary mode ignores value 0
+ *     (bendabir.com, "The basic approach": background keeps 0).
+ *
+ * Algorithm: for every image, scan the pixels in raster order; every pixel
+ * that is neither labelled nor ignored starts a new region with the next
+ * number and a breadth-first flood fill (explicit FIFO queue, no recursion)
+ * spreads that number over every pixel reachable through equal-valued
+ * neighbours.  Because the seeds are taken in raster order, the first pixel
+ * of every region is its seed, and the numbering is the canonical one.
+ *
+ * Equality compares all pixel_bytes bytes of a pixel (RGBA: alpha included).
+ */
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* Return codes mirror the library's status numbers where they overlap. */
+#define ORACLE_OK 0
+#define ORACLE_ERR_INVALID_ARG 1
+#define ORACLE_ERR_NO_MEMORY 4
+
+enum { ORACLE_MODE_ALL = 0, ORACLE_MODE_BINARY = 1 };
+
+static int same_value(const uint8_t* a, const uint8_t* b, int pb) {
+  return memcmp(a, b, (size_t)pb) == 0;
+}
+
+static int is_zero(const uint8_t* a, int pb) {
+  for (int k = 0; k < pb; ++k)
+    if (a[k] != 0) return 0;
+  return 1;
+}
+
+/*
+ * Label one image.  img: H*W pixels of pb bytes, row-major.  labels: H*W
+ * int32, written completely.  queue: scratch of H*W int64.  Returns the
+ * number of regions.
+ */
+static int64_t label_one(const uint8_t* img, int64_t H, int64_t W, int pb,
+                         int conn, int mode, int32_t* labels, int64_t* queue) {
+  const int64_t N = H * W;
+  /* neighbour offsets: 4-connectivity uses the first four (edge-sharing),
+   * 8-connectivity adds the four corner-sharing ones */
+  static const int dr[8] = {-1, 0, 0, 1, -1, -1, 1, 1};
+  static const int dc[8] = {0, -1, 1, 0, -1, 1, -1, 1};
+  const int nn = (conn == 8) ? 8 : 4;
+
+  for (int64_t i = 0; i < N; ++i) labels[i] = 0;
+  /* pixels still to visit are marked -1; ignored pixels keep 0 */
+  for (int64_t i = 0; i < N; ++i) {
+    const uint8_t* v = img + i * pb;
+    if (mode == ORACLE_MODE_BINARY && is_zero(v, pb))
+      labels[i] = 0;
+    else
+      labels[i] = -1;
+  }
+
+  int64_t n = 0;
+  for (int64_t seed = 0; seed < N; ++seed) {
+    if (labels[seed] != -1) continue;
+    ++n;
+    labels[seed] = (int32_t)n;
+    int64_t head = 0, tail = 0;
+    queue[tail++] = seed;
+    while (head < tail) {
+      const int64_t p = queue[head++];
+      const int64_t r = p / W, c = p % W;
+      const uint8_t* pv = img + p * pb;
+      for (int k = 0; k < nn; ++k) {
+        const int64_t rr = r + dr[k], cc = c + dc[k];
+        if (rr < 0 || rr >= H || cc < 0 || cc >= W) continue; /* no wrap */
+        const int64_t q = rr * W + cc;
+        if (labels[q] != -1) continue;
+        if (!same_value(pv, img + q * pb, pb)) continue;
+        labels[q] = (int32_t)n;
+        queue[tail++] = q;
+      }
+    }
+  }
+  return n;
+}
+
+/*
+ * oracle_label: label `batch` images of H x W pixels of `pixel_bytes` bytes,
+ * stored contiguously; image b starts at byte b*H*W*pixel_bytes and its labels
+ * at element b*H*W.  n_out[b] receives the number of regions of image b.
+ * Host pointers only.  Returns ORACLE_OK, ORACLE_ERR_INVALID_ARG or
+ * ORACLE_ERR_NO_MEMORY.
+ */
+int oracle_label(const void* img, int64_t batch, int64_t H, int64_t W,
+                 int pixel_bytes, int connectivity, int mode,
+                 int32_t* labels, int32_t* n_out) {
+  if (batch < 0 || H < 0 || W < 0) return ORACLE_ERR_INVALID_ARG;
+  if (pixel_bytes < 1 || pixel_bytes > 16) return ORACLE_ERR_INVALID_ARG;
+  if (connectivity != 4 && connectivity != 8) return ORACLE_ERR_INVALID_ARG;
+  if (mode != ORACLE_MODE_ALL && mode != ORACLE_MODE_BINARY)
+    return ORACLE_ERR_INVALID_ARG;
+  const int64_t N = H * W;
+  if (batch == 0 || N == 0) {
+    for (int64_t b = 0; b < batch; ++b) n_out[b] = 0;
+    return ORACLE_OK;
+  }
+  if (!img || !labels || !n_out) return ORACLE_ERR_INVALID_ARG;
+  if (N >= ((int64_t)1 << 31)) return ORACLE_ERR_INVALID_ARG;
+  int64_t* queue = (int64_t*)malloc((size_t)N * sizeof(int64_t));
+  if (!queue) return ORACLE_ERR_NO_MEMORY;
+  const uint8_t* base = (const uint8_t*)img;
+  for (int64_t b = 0; b < batch; ++b) {
+    n_out[b] = (int32_t)label_one(base + b * N * pixel_bytes, H, W,
+                                  pixel_bytes, connectivity, mode,
+                                  labels + b * N, queue);
+  }
+  free(queue);
+  return ORACLE_OK;
+}
