@@ -1,0 +1,173 @@
+"""GB300 connected-component labelling: thin Python binding over libccl.so.
+
+Every step of the labelling runs in the CUDA kernels of ``csrc/ccl.cu``; this
+module only marshals arguments to the C ABI declared in ``include/ccl.h``.
+PyTorch is used for device memory and the current stream.  There is no CPU
+path: if the compiled library is missing, every call raises.
+
+Names follow the C ABI (``ccl_label``, ``ccl_label_ws``, ``ccl_label_host``,
+``ccl_workspace_bytes``, ``ccl_last_status``, ``ccl_status_string``,
+``ccl_set_option``); ``label`` is the tensor-level convenience wrapper.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from ._build import LIB_PATH, build  # noqa: F401
+
+CCL_OK = 0
+CCL_ERR_INVALID_ARG = 1
+CCL_ERR_TOO_LARGE = 2
+CCL_ERR_CUDA = 3
+CCL_ERR_NO_MEMORY = 4
+CCL_ERR_DEVICE_LIMIT = 5
+CCL_MODE_ALL = 0
+CCL_MODE_BINARY = 1
+CCL_OPT_WALK_CAP = 1
+
+# every symbol include/ccl.h declares
+EXPORTED = ("ccl_label", "ccl_workspace_bytes", "ccl_label_ws", "ccl_label_host",
+            "ccl_last_status", "ccl_status_string", "ccl_set_option", "ccl_version")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class CCLError(RuntimeError):
+    def __init__(self, status, what=""):
+        self.status = status
+        super().__init__("%s%s" % (what + ": " if what else "", ccl_status_string(status)))
+
+
+def lib():
+    """The loaded libccl.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError("libccl.so is not built (%s); run "
+                                   "connected_component_labelling_gb300.build()" % LIB_PATH)
+            L = ctypes.CDLL(LIB_PATH)
+            vp, i32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+            L.ccl_label.argtypes = [vp, i32, i32, i32, i32, i32, i32, vp, vp, vp]
+            L.ccl_label.restype = i32
+            L.ccl_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, i32]
+            L.ccl_workspace_bytes.restype = sz
+            L.ccl_label_ws.argtypes = [vp, i32, i32, i32, i32, i32, i32, vp, vp, vp, sz, vp]
+            L.ccl_label_ws.restype = i32
+            L.ccl_label_host.argtypes = [vp, i32, i32, i32, i32, i32, i32, vp, vp, vp]
+            L.ccl_label_host.restype = i32
+            L.ccl_last_status.argtypes = [vp]
+            L.ccl_last_status.restype = i32
+            L.ccl_status_string.argtypes = [i32]
+            L.ccl_status_string.restype = ctypes.c_char_p
+            L.ccl_set_option.argtypes = [i32, ctypes.c_longlong]
+            L.ccl_set_option.restype = i32
+            L.ccl_version.argtypes = []
+            L.ccl_version.restype = i32
+            _lib = L
+    return _lib
+
+
+# ------------------------------------------------------------ raw C-ABI calls
+
+def ccl_label(img, batch, H, W, pixel_bytes, connectivity, mode, labels, n_regions, stream):
+    return lib().ccl_label(img, batch, H, W, pixel_bytes, connectivity, mode, labels,
+                           n_regions, stream)
+
+
+def ccl_workspace_bytes(batch, H, W, pixel_bytes, connectivity, mode):
+    return lib().ccl_workspace_bytes(batch, H, W, pixel_bytes, connectivity, mode)
+
+
+def ccl_label_ws(img, batch, H, W, pixel_bytes, connectivity, mode, labels, n_regions,
+                 workspace, workspace_bytes, stream):
+    return lib().ccl_label_ws(img, batch, H, W, pixel_bytes, connectivity, mode, labels,
+                              n_regions, workspace, workspace_bytes, stream)
+
+
+def ccl_label_host(img, batch, H, W, pixel_bytes, connectivity, mode, labels, n_regions,
+                   stream):
+    return lib().ccl_label_host(img, batch, H, W, pixel_bytes, connectivity, mode, labels,
+                                n_regions, stream)
+
+
+def ccl_last_status(stream=None):
+    return lib().ccl_last_status(stream)
+
+
+def ccl_status_string(status):
+    return lib().ccl_status_string(int(status)).decode()
+
+
+def ccl_set_option(option, value):
+    return lib().ccl_set_option(option, value)
+
+
+def ccl_version():
+    return lib().ccl_version()
+
+
+# ------------------------------------------------------------ tensor wrapper
+
+_MODES = {"all": CCL_MODE_ALL, "binary": CCL_MODE_BINARY,
+          CCL_MODE_ALL: CCL_MODE_ALL, CCL_MODE_BINARY: CCL_MODE_BINARY}
+
+
+def image_geometry(img):
+    """(batch, H, W, pixel_bytes, squeeze) of a [B,]H,W tensor of 1/2/4-byte
+    pixels, or a [B,]H,W,C uint8 tensor whose C bytes form one pixel."""
+    import torch
+    if img.dtype == torch.uint8 and img.dim() == 4 and img.shape[-1] in (2, 4):
+        B, H, W, pb = img.shape
+        return B, H, W, pb, False
+    pb = img.element_size()
+    if img.dim() == 3:
+        B, H, W = img.shape
+        return B, H, W, pb, False
+    if img.dim() == 2:
+        H, W = img.shape
+        return 1, H, W, pb, True
+    raise ValueError("expected a [B,]H,W tensor")
+
+
+def label(img, connectivity=8, mode="all", out=None, n_out=None, workspace=None, stream=None):
+    """Label a CUDA tensor of images.  Returns (labels int32 tensor shaped like
+    the pixel grid, n_regions int32 tensor [B] (0-d for a 2-D input)).
+    Asynchronous on ``stream`` (default: torch's current stream)."""
+    import torch
+    if not img.is_cuda:
+        raise ValueError("label() needs a CUDA tensor; the library has no CPU path")
+    img = img.contiguous()
+    B, H, W, pb, squeeze = image_geometry(img)
+    m = _MODES[mode]
+    if out is None:
+        out = torch.empty((B, H, W), dtype=torch.int32, device=img.device)
+    if n_out is None:
+        n_out = torch.empty((B,), dtype=torch.int32, device=img.device)
+    st = stream if stream is not None else torch.cuda.current_stream(img.device)
+    sp = st.cuda_stream
+    with torch.cuda.device(img.device):
+        if workspace is None:
+            rc = ccl_label(img.data_ptr(), B, H, W, pb, connectivity, m, out.data_ptr(),
+                           n_out.data_ptr(), sp)
+        else:
+            rc = ccl_label_ws(img.data_ptr(), B, H, W, pb, connectivity, m, out.data_ptr(),
+                              n_out.data_ptr(), workspace.data_ptr(),
+                              workspace.numel() * workspace.element_size(), sp)
+    if rc != CCL_OK:
+        raise CCLError(rc, "ccl_label")
+    if squeeze:
+        return out.view(H, W), n_out.view(())
+    return out, n_out
+
+
+def check_status(stream=None):
+    """Synchronise ``stream`` and raise if a device-side limit tripped."""
+    import torch
+    st = stream if stream is not None else torch.cuda.current_stream()
+    rc = ccl_last_status(st.cuda_stream)
+    if rc != CCL_OK:
+        raise CCLError(rc, "device status")

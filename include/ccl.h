@@ -1,0 +1,141 @@
+/*
+ * ccl.h -- C ABI of the GB300 connected-component labelling library
+ * (libccl.so).
+ *
+ * The operation ("every-colour", blogs.fablnx.com, ch. 01 "The job" and
+ * ch. 02 "Regions"): two pixels belong to the same region exactly when a path
+ * of neighbouring pixels of exactly equal value joins them; 8-connectivity
+ * counts corner-sharing neighbours, 4-connectivity only edge-sharing ones
+ * ("About Connected Components Labeling on GPU", bendabir.com, Prologue).
+ * Regions are numbered 1..n in the raster order of their first pixel
+ * ("every-colour", ch. 04 "Point at a leader" -- the leader is the first
+ * pixel in reading order -- and ch. 11 "How we know it is right").  In
+ * binary mode value 0 is background: it keeps label 0 and joins nothing
+ * ("every-colour", ch. 08 switch 4 "Ignore the paper"; bendabir.com, "The
+ * basic approach", labels + 1 keep 0 for background).
+ *
+ * The library runs the four stages of "every-colour" ch. 05 (Start,
+ * Connect, Collapse, Number) as CUDA kernels for sm_103a.  There is no CPU
+ * fallback: every entry point that computes needs a CUDA device.
+ *
+ * Conventions for every entry point:
+ *  - Images are contiguous and row-major: pixel (b, y, x) sits at byte
+ *    ((b*H + y)*W + x) * pixel_bytes of `img`; labels likewise at element
+ *    (b*H + y)*W + x of `labels_i32`.  `img` must be aligned to pixel_bytes,
+ *    `labels_i32` and `n_regions_out` to 4 bytes.
+ *  - Pixel equality compares all pixel_bytes bytes (RGBA: alpha included).
+ *  - Labels are canonical per image: numbering restarts at 1 in every image.
+ *  - H*W must be below 2^31 (CCL_ERR_TOO_LARGE otherwise); batch*H*W may
+ *    exceed it.
+ *  - batch == 0, H == 0 or W == 0 is a valid empty call (n_regions_out, if
+ *    given, is set to 0 for every image).
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL is the legacy
+ *    default stream).  The return value reports argument and launch errors
+ *    only; a device-side limit that trips is reported by ccl_last_status().
+ *  - `labels_i32` doubles as the union-find parent array while the call
+ *    runs ("every-colour", ch. 09: the labels are the only per-pixel memory),
+ *    so it must not overlap `img`.
+ *  - All pointers are owned by the caller; the library frees nothing of theirs.
+ */
+#ifndef CCL_H_
+#define CCL_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same layout as cudaStream_t, without pulling in the CUDA headers. */
+typedef struct CUstream_st* ccl_stream_t;
+
+typedef enum {
+  CCL_OK = 0,
+  CCL_ERR_INVALID_ARG = 1,   /* bad pointer, size, enum value or alignment */
+  CCL_ERR_TOO_LARGE = 2,     /* H*W >= 2^31 */
+  CCL_ERR_CUDA = 3,          /* a CUDA runtime call or launch failed */
+  CCL_ERR_NO_MEMORY = 4,     /* workspace allocation failed / too small */
+  CCL_ERR_DEVICE_LIMIT = 5   /* a bounded device loop reached its cap */
+} ccl_status;
+
+enum { CCL_MODE_ALL = 0, CCL_MODE_BINARY = 1 };
+
+/*
+ * ccl_label -- label `batch` images of H x W pixels.
+ *   img            device pointer, batch*H*W pixels of pixel_bytes (1, 2 or 4)
+ *   connectivity   4 or 8
+ *   mode           CCL_MODE_ALL (every pixel labelled) or CCL_MODE_BINARY
+ *                  (all-zero pixels are background, label 0)
+ *   labels_i32     device pointer, batch*H*W int32, written completely
+ *   n_regions_out  device pointer to batch int32 (region count per image),
+ *                  or NULL
+ * Scratch (about H*W/256*4 + H*ceil(W/32)*4 bytes per image) comes from a
+ * stream-ordered memory pool the library keeps per device.
+ * Returns CCL_OK or an error status; nothing is written on an argument error.
+ */
+int ccl_label(const void* img, int batch, int H, int W, int pixel_bytes,
+              int connectivity, int mode, int32_t* labels_i32,
+              int32_t* n_regions_out, ccl_stream_t stream);
+
+/* Bytes of device workspace ccl_label_ws needs for these arguments
+ * (0 for an empty call or invalid arguments). */
+size_t ccl_workspace_bytes(int batch, int H, int W, int pixel_bytes,
+                           int connectivity, int mode);
+
+/*
+ * ccl_label_ws -- ccl_label with caller-provided scratch: `workspace` is a
+ * device pointer to at least ccl_workspace_bytes(...) bytes, 256-byte
+ * aligned, owned by the caller and not used by any other call in flight.
+ * Returns CCL_ERR_NO_MEMORY if workspace_bytes is too small.
+ */
+int ccl_label_ws(const void* img, int batch, int H, int W, int pixel_bytes,
+                 int connectivity, int mode, int32_t* labels_i32,
+                 int32_t* n_regions_out, void* workspace,
+                 size_t workspace_bytes, ccl_stream_t stream);
+
+/*
+ * ccl_label_host -- the whole call from host memory: copies `img_host` to
+ * the device, labels it and copies the labels (and counts) back into
+ * `labels_host` / `n_regions_host` (host pointers; page-locked memory is
+ * fastest).  Device buffers come from the library's pool.  Returns after the
+ * results are in host memory (the stream is synchronised); a tripped device
+ * limit is returned directly as CCL_ERR_DEVICE_LIMIT.
+ */
+int ccl_label_host(const void* img_host, int batch, int H, int W,
+                   int pixel_bytes, int connectivity, int mode,
+                   int32_t* labels_host, int32_t* n_regions_host,
+                   ccl_stream_t stream);
+
+/*
+ * ccl_last_status -- synchronises `stream`, then returns and clears the
+ * current device's sticky device-side status: CCL_ERR_DEVICE_LIMIT if a
+ * bounded loop (a union-find walk or a union retry) reached its cap in any
+ * call since the last check, CCL_ERR_CUDA if the stream reports an error,
+ * else CCL_OK.  The caps are far above any legitimate walk; tripping one
+ * means the labels of that call are not valid.
+ */
+int ccl_last_status(ccl_stream_t stream);
+
+/* Human-readable name of a status value (static string). */
+const char* ccl_status_string(int status);
+
+/*
+ * Debug / test options (process-wide):
+ *   CCL_OPT_WALK_CAP  cap on every union-find walk and union retry loop
+ *                     (value <= 0 restores the default, the number of pixels
+ *                     the walk can visit); lowering it lets a test make the
+ *                     device report CCL_ERR_DEVICE_LIMIT without any hang.
+ * Returns CCL_OK or CCL_ERR_INVALID_ARG for an unknown option.
+ */
+enum { CCL_OPT_WALK_CAP = 1 };
+int ccl_set_option(int option, long long value);
+
+/* Library version, as major*10000 + minor*100 + patch. */
+int ccl_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CCL_H_ */

@@ -1,0 +1,108 @@
+"""CPU-only checks of the C ABI: the library builds, loads, exports every
+symbol include/ccl.h declares, and rejects bad arguments on the host before
+touching any device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import connected_component_labelling_gb300 as ccl
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                      "include", "ccl.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    ccl.build()
+    return ccl.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^[A-Za-z_][\w \*]*?\b(ccl_\w+)\s*\(", text, re.M)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("ccl_label", "ccl_label_ws", "ccl_workspace_bytes", "ccl_label_host",
+              "ccl_last_status", "ccl_status_string", "ccl_set_option", "ccl_version"):
+        assert n in names
+    assert sorted(ccl.EXPORTED) == names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    # dynamic symbol table, checked through dlsym
+    handle = ctypes.CDLL(ccl.LIB_PATH)
+    for name in declared_functions():
+        assert ctypes.cast(getattr(handle, name), ctypes.c_void_p).value
+
+
+def test_status_strings_and_version(lib):
+    assert ccl.ccl_status_string(ccl.CCL_OK) == "CCL_OK"
+    assert ccl.ccl_status_string(ccl.CCL_ERR_DEVICE_LIMIT) == "CCL_ERR_DEVICE_LIMIT"
+    assert ccl.ccl_status_string(99) == "CCL_ERR_UNKNOWN"
+    assert ccl.ccl_version() >= 100
+
+
+def test_workspace_bytes(lib):
+    assert ccl.ccl_workspace_bytes(0, 10, 10, 1, 8, 0) == 0
+    assert ccl.ccl_workspace_bytes(1, 10, 10, 3, 8, 0) == 0       # bad pixel_bytes
+    assert ccl.ccl_workspace_bytes(1, 10, 10, 1, 6, 0) == 0       # bad connectivity
+    assert ccl.ccl_workspace_bytes(1, 1 << 16, 1 << 15, 1, 8, 0) == 0   # H*W = 2^31
+    a = ccl.ccl_workspace_bytes(1, 1024, 1024, 4, 8, 0)
+    b = ccl.ccl_workspace_bytes(2, 1024, 1024, 4, 8, 0)
+    assert 0 < a < b
+    # bitmap (1 bit/px) + one count per 256 px, rounded: far below the labels
+    assert a < 1024 * 1024 // 4
+    assert a % 256 == 0
+
+
+FAKE = 1 << 20   # a host address never dereferenced: validation fails first
+
+
+@pytest.mark.parametrize("args,expect", [
+    ((FAKE, 1, 8, 8, 3, 8, 0), ccl.CCL_ERR_INVALID_ARG),     # pixel_bytes
+    ((FAKE, 1, 8, 8, 1, 6, 0), ccl.CCL_ERR_INVALID_ARG),     # connectivity
+    ((FAKE, 1, 8, 8, 1, 8, 2), ccl.CCL_ERR_INVALID_ARG),     # mode
+    ((FAKE, -1, 8, 8, 1, 8, 0), ccl.CCL_ERR_INVALID_ARG),    # batch
+    ((FAKE, 1, -8, 8, 1, 8, 0), ccl.CCL_ERR_INVALID_ARG),    # H
+    ((None, 1, 8, 8, 1, 8, 0), ccl.CCL_ERR_INVALID_ARG),     # null image
+    ((FAKE + 1, 1, 8, 8, 4, 8, 0), ccl.CCL_ERR_INVALID_ARG), # misaligned RGBA
+    ((FAKE, 1, 1 << 16, 1 << 15, 1, 8, 0), ccl.CCL_ERR_TOO_LARGE),
+])
+def test_invalid_arguments_rejected_on_host(lib, args, expect):
+    img, B, H, W, pb, conn, mode = args
+    labels = FAKE * 64
+    assert ccl.ccl_label(img, B, H, W, pb, conn, mode, labels, None, None) == expect
+    assert ccl.ccl_label_ws(img, B, H, W, pb, conn, mode, labels, None, FAKE * 128, 1 << 20,
+                            None) == expect
+
+
+def test_null_labels_and_overlap_rejected(lib):
+    assert ccl.ccl_label(FAKE, 1, 8, 8, 1, 8, 0, None, None, None) == ccl.CCL_ERR_INVALID_ARG
+    # labels overlapping the image
+    assert ccl.ccl_label(FAKE, 1, 8, 8, 4, 8, 0, FAKE + 64, None, None) == ccl.CCL_ERR_INVALID_ARG
+
+
+def test_workspace_checks_on_host(lib):
+    need = ccl.ccl_workspace_bytes(1, 64, 64, 1, 8, 0)
+    args = (FAKE, 1, 64, 64, 1, 8, 0, FAKE * 64, None)
+    assert ccl.ccl_label_ws(*args, FAKE * 128, need - 1, None) == ccl.CCL_ERR_NO_MEMORY
+    assert ccl.ccl_label_ws(*args, FAKE * 128 + 16, need, None) == ccl.CCL_ERR_INVALID_ARG
+    assert ccl.ccl_label_ws(*args, None, need, None) == ccl.CCL_ERR_INVALID_ARG
+
+
+def test_set_option(lib):
+    assert ccl.ccl_set_option(ccl.CCL_OPT_WALK_CAP, 5) == ccl.CCL_OK
+    assert ccl.ccl_set_option(ccl.CCL_OPT_WALK_CAP, 0) == ccl.CCL_OK
+    assert ccl.ccl_set_option(12345, 1) == ccl.CCL_ERR_INVALID_ARG
+
+
+def test_no_cpu_path():
+    import torch
+    with pytest.raises(ValueError):
+        ccl.label(torch.zeros((4, 4), dtype=torch.uint8))
