@@ -1,0 +1,429 @@
+#!/usr/bin/env python
+"""Benchmark: Gpixel/s labelled (device-timed) and % of the HBM roofline.
+
+Default workload: the 806.4-Mpixel construction-sheet analogue (24000 rows x
+33600 columns, RGBA, 8-connectivity, every pixel labelled) -- the workload the
+headline target is quoted on.  One step is one ccl_label call over the whole
+sheet (all four stages: Start, Connect, Collapse, Number).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+                    [--workload c0|c1|c2|c3:<structure>:<conn>:<mode>|c4]
+
+Prints ONE JSON line (rank 0).  Device time: CUDA events on the launching
+stream around exactly K steps, inputs resident in HBM.  Per-stage times come
+from CUDA events the library records on the same stream (option
+CCL_OPT_STAGE_EVENTS).  e2e: the same metric through ccl_label_host with
+page-locked host buffers, host<->device copies inside the timed region.
+cpu_baseline / --impl reference: the oracle (single-threaded BFS) on a band of
+the same sheet, on this machine's host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "Gpixel/s labelled (device-timed) and % of HBM roofline, 1 GB300"
+UNIT = "Gpixel/s"
+FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 129 * 1024 * 1024
+REF_ROWS = 1200           # rows of the sheet one reference step labels
+CPU_BASELINE_ROWS = 9600  # rows of the sheet the cpu_baseline leg labels
+
+
+# ------------------------------------------------------------------ workloads
+
+def make_workload(name, device):
+    """Returns (config dict, device tensor [B,H,W] or [H,W], pb, conn, mode)."""
+    import workloads as wl
+    if name == "c4":
+        img = wl.c4_sheet(device=device)
+        return (dict(workload="c4_sheet_24000x33600_rgba", batch=1, H=wl.C4_H, W=wl.C4_W,
+                     pixel_bytes=4, connectivity=8, mode="all"), img, 4, 8, 0)
+    if name == "c0":
+        img = wl.c0_drawing(device=device)
+        return (dict(workload="c0_drawing_1024_rgba", batch=1, H=1024, W=1024, pixel_bytes=4,
+                     connectivity=8, mode="all"), img, 4, 8, 0)
+    if name == "c1":
+        img = wl.c1_masks(device=device)
+        return (dict(workload="c1_masks_64x1024x1024_u8", batch=64, H=1024, W=1024,
+                     pixel_bytes=1, connectivity=8, mode="binary"), img, 1, 8, 1)
+    if name == "c2":
+        img = wl.c2_slide(device=device)
+        return (dict(workload="c2_slide_20000x20000_u8", batch=1, H=20000, W=20000,
+                     pixel_bytes=1, connectivity=4, mode="binary"), img, 1, 4, 1)
+    if name.startswith("c3"):
+        _, structure, conn, mode = name.split(":")
+        img = wl.c3_structures(device=device)[structure]
+        m = 1 if mode == "binary" else 0
+        return (dict(workload="c3_%s_8192x8192_u8" % structure, batch=1, H=8192, W=8192,
+                     pixel_bytes=1, connectivity=int(conn), mode=mode), img, 1, int(conn), m)
+    raise SystemExit("unknown workload %r" % name)
+
+
+def sheet_band(rows, device="cpu"):
+    import workloads as wl
+    return wl.c4_sheet(device=device, rows=(0, rows))
+
+
+# ------------------------------------------------------------------ helpers
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def source_sha():
+    h = hashlib.sha256()
+    with open(os.path.join(ROOT, "connected_component_labelling_gb300", "csrc", "ccl.cu"), "rb") as f:
+        h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_per_px(kernel, workload):
+    """DRAM bytes per pixel of `kernel` from the committed ncu summary, or
+    None when the kernel source changed since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            t = json.load(f)
+    except Exception:
+        return None
+    if t.get("source_sha") != source_sha():
+        return None
+    ent = t.get("kernels", {}).get(workload, {}).get(kernel)
+    return None if ent is None else float(ent)
+
+
+class ClockSampler:
+    """nvidia-smi samples (every 200 ms) of the GPU this rank uses; keeps
+    the arrival time of every line so samples can be matched to a region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.rows = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append((time.time(), [s.strip() for s in line.split(",")]))
+
+    def wait_first(self, timeout=10.0):
+        t0 = time.time()
+        while self.proc and not self.rows and time.time() - t0 < timeout:
+            time.sleep(0.02)
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        inside = [r for (t, r) in self.rows if t0 <= t <= t1 + 0.2]
+        note = "inside the timed region"
+        if not inside:   # region shorter than the sampling period: nearest samples
+            inside = [r for (t, r) in self.rows if t0 - 0.5 <= t <= t1 + 0.5]
+            note = "within 0.5 s of the timed region (region shorter than the 200 ms period)"
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in inside:
+            try:
+                sm.append(float(r[1])); mx.append(float(r[2]))
+            except Exception:
+                continue
+            for k, nm in enumerate(names):
+                if len(r) > 5 + k and r[5 + k].lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm), "window": note}
+
+
+def dist_setup(args):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if (torch.cuda.is_available() and args.impl != "reference") else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def max_over_ranks(value, world):
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------------------ oracle legs
+
+def time_oracle(img_np, conn, mode):
+    import oracle
+    t0 = time.perf_counter()
+    oracle.label(img_np, conn, mode)
+    return time.perf_counter() - t0
+
+
+def run_reference(args, world, rank):
+    """The oracle as it stands, timed on this machine's host cores, one step =
+    one labelling of a REF_ROWS-row band of the sheet."""
+    if rank != 0:
+        return
+    import numpy as np
+    import oracle
+    oracle.build()
+    band = sheet_band(REF_ROWS).numpy().view(np.uint32)
+    px = band.size
+    for _ in range(args.warmup):
+        time_oracle(band, 8, oracle.MODE_ALL)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        time_oracle(band, 8, oracle.MODE_ALL)
+    dt = (time.perf_counter() - t0) / max(1, args.steps)
+    gpxs = px / dt / 1e9
+    sample = "rows 0-%d of the 24000 x 33600 sheet (%d px) per step, single thread" % (REF_ROWS, px)
+    line = {"impl": "reference", "metric": METRIC, "value": gpxs, "unit": UNIT,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "int32", "data": "synthetic",
+            "config": {"workload": "c4_sheet_24000x33600_rgba", "batch": 1, "H": 24000,
+                       "W": 33600, "pixel_bytes": 4, "connectivity": 8, "mode": "all",
+                       "sample_rows": REF_ROWS},
+            "cpu_baseline": {"value": gpxs, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": gpxs, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ main arm
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ccl", choices=["ccl", "reference"])
+    ap.add_argument("--workload", default="c4")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+
+    world, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        return
+
+    import numpy as np
+    import torch
+    import connected_component_labelling_gb300 as ccl
+
+    ccl.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    cfg, img, pb, conn, mode = make_workload(args.workload, dev)
+    img = img.contiguous()
+    B, H, W = cfg["batch"], cfg["H"], cfg["W"]
+    px = B * H * W
+    labels = torch.empty(px, dtype=torch.int32, device=dev)
+    nreg = torch.empty(B, dtype=torch.int32, device=dev)
+    wsb = ccl.ccl_workspace_bytes(B, H, W, pb, conn, mode)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sp = stream.cuda_stream
+
+    def step():
+        rc = ccl.ccl_label_ws(img.data_ptr(), B, H, W, pb, conn, mode, labels.data_ptr(),
+                              nreg.data_ptr(), ws.data_ptr(), wsb, sp)
+        if rc != ccl.CCL_OK:
+            raise ccl.CCLError(rc, "ccl_label_ws")
+
+    for _ in range(args.warmup):
+        step()
+    ccl.check_status(stream)
+
+    small = (px * (pb + 4)) < 2 * L2_BYTES
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.int32, device=dev) if small else None
+    gpu_index = local
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        ids = [s for s in vis.split(",") if s.strip()]
+        if local < len(ids):
+            gpu_index = ids[local]
+    sampler = ClockSampler(gpu_index)
+    sampler.wait_first()
+
+    ccl.ccl_stage_times()                       # forget anything recorded before
+    ccl.ccl_set_option(ccl.CCL_OPT_STAGE_EVENTS, 1)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    launches0 = ccl.ccl_kernel_launches()
+    t_wall0 = time.time()
+    if not small:
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        total_ms = e0.elapsed_time(e1)
+    else:
+        # inputs fit in L2: flush it between steps, outside the timed events
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        for a, b in evs:
+            flush.fill_(1)
+            a.record(stream)
+            step()
+            b.record(stream)
+        torch.cuda.synchronize(dev)
+        total_ms = sum(a.elapsed_time(b) for a, b in evs)
+    t_wall1 = time.time()
+    launches = ccl.ccl_kernel_launches() - launches0
+    barrier(world)
+    ccl.ccl_set_option(ccl.CCL_OPT_STAGE_EVENTS, 0)
+    sampler.stop()
+    ccl.check_status(stream)
+    stage_ms, ncalls = ccl.ccl_stage_times()
+    ms = total_ms / args.steps
+    ms_max = max_over_ranks(ms, world)
+    value = world * px / (ms_max * 1e-3) / 1e9
+    clocks = sampler.summary(t_wall0, t_wall1)
+    n_regions = nreg.cpu().tolist()
+
+    # ---- roofline
+    peak, peak_kind = load_peaks()
+    names = [ccl.ccl_stage_name(k) for k in range(len(stage_ms))]
+    per_call = [s / max(1, ncalls) for s in stage_ms]
+    # algorithmic bytes per pixel of each stage that streams the image
+    alg = {"tile_local": pb + 4, "number": 4 + 4}
+    dom = max(range(len(per_call)), key=lambda k: per_call[k]) if per_call else 0
+    dom_name = names[dom] if names else "tile_local"
+    dom_alg = alg.get(dom_name)
+    stages = {}
+    for k, nm in enumerate(names):
+        ent = {"ms": per_call[k], "share": per_call[k] / sum(per_call) if sum(per_call) else None}
+        if nm in alg:
+            gbs = alg[nm] * px / (per_call[k] * 1e-3) / 1e9 if per_call[k] > 0 else None
+            ent.update({"alg_bytes_per_px": alg[nm], "achieved_gbs": gbs,
+                        "frac": gbs / peak if gbs else None})
+        stages[nm] = ent
+    if dom_alg is None:
+        dom_alg = 0
+    achieved = dom_alg * px / (per_call[dom] * 1e-3) / 1e9 if per_call and per_call[dom] > 0 else None
+    tpp = traffic_per_px(dom_name, cfg["workload"])
+    roofline = {"bound": "hbm", "kernel": dom_name, "achieved": achieved, "peak": peak,
+                "unit": "GB/s", "frac": (achieved / peak) if achieved else None,
+                "traffic": (tpp * px) if tpp is not None else None,
+                "alg_bytes": dom_alg * px, "peak_source": peak_kind + " (MEASURED_PEAKS.json hbm_gbs)"
+                if peak_kind == "measured" else "fallback 6.8 TB/s"}
+    path_gbs = (pb + 4) * px / (ms * 1e-3) / 1e9
+    roofline_path = {"bound": "hbm", "alg_bytes_per_px": pb + 4, "achieved": path_gbs,
+                     "peak": peak, "unit": "GB/s", "frac": path_gbs / peak,
+                     "note": "whole ccl_label call: image read once + int32 label write"}
+
+    # ---- e2e through the host entry point
+    e2e = None
+    if not args.no_e2e:
+        himg = img.cpu().contiguous().pin_memory()
+        hlab = torch.empty(px, dtype=torch.int32).pin_memory()
+        hn = torch.empty(B, dtype=torch.int32).pin_memory()
+        rc = ccl.ccl_label_host(himg.data_ptr(), B, H, W, pb, conn, mode, hlab.data_ptr(),
+                                hn.data_ptr(), sp)      # warm the pool
+        if rc != ccl.CCL_OK:
+            raise ccl.CCLError(rc, "ccl_label_host")
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        t0 = time.perf_counter()
+        for _ in range(args.e2e_steps):
+            rc = ccl.ccl_label_host(himg.data_ptr(), B, H, W, pb, conn, mode, hlab.data_ptr(),
+                                    hn.data_ptr(), sp)
+            if rc != ccl.CCL_OK:
+                raise ccl.CCLError(rc, "ccl_label_host")
+        dt = (time.perf_counter() - t0) / args.e2e_steps
+        dt = max_over_ranks(dt, world)
+        same = bool(torch.equal(hlab, labels.cpu()))
+        e2e = {"value": world * px / dt / 1e9, "unit": UNIT, "ms_per_step": dt * 1e3,
+               "h2d_bytes_per_step": px * pb, "d2h_bytes_per_step": px * 4 + B * 4,
+               "steps": args.e2e_steps, "api": "ccl_label_host (pinned host buffers)",
+               "labels_match_device_run": same}
+        del himg, hlab
+
+    # ---- cpu baseline: the oracle on a band of the sheet, this host, 1 thread
+    cpu_baseline = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and args.workload == "c4":
+        import oracle
+        oracle.build()
+        band = img[:CPU_BASELINE_ROWS].cpu().numpy().view(np.uint32)
+        dt = time_oracle(band, 8, oracle.MODE_ALL)
+        cpu_baseline = {"value": band.size / dt / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
+                        "sample": "rows 0-%d of the sheet (%d px), one single-threaded BFS pass, "
+                                  "%.1f s" % (CPU_BASELINE_ROWS, band.size, dt)}
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "int32", "data": "synthetic",
+                "config": dict(cfg, l2=("L2 flushed between steps (outside the events)" if small
+                                        else "inputs larger than L2 (%.2f GB moved per step)"
+                                        % (px * (pb + 4) / 1e9)),
+                               parallelism="replicas" if world > 1 else "single"),
+                "roofline": roofline, "roofline_path": roofline_path, "stages": stages,
+                "cpu_baseline": cpu_baseline, "e2e": e2e, "gpu_launches": launches,
+                "clocks": clocks, "n_regions": n_regions[:8],
+                "kernel_source_sha": source_sha()}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

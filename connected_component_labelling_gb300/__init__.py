@@ -26,10 +26,12 @@ CCL_ERR_DEVICE_LIMIT = 5
 CCL_MODE_ALL = 0
 CCL_MODE_BINARY = 1
 CCL_OPT_WALK_CAP = 1
+CCL_OPT_STAGE_EVENTS = 2
 
 # every symbol include/ccl.h declares
 EXPORTED = ("ccl_label", "ccl_workspace_bytes", "ccl_label_ws", "ccl_label_host",
-            "ccl_last_status", "ccl_status_string", "ccl_set_option", "ccl_version")
+            "ccl_last_status", "ccl_status_string", "ccl_set_option", "ccl_stage_times",
+            "ccl_stage_name", "ccl_kernel_launches", "ccl_version")
 
 _lock = threading.Lock()
 _lib = None
@@ -65,6 +67,12 @@ def lib():
             L.ccl_status_string.restype = ctypes.c_char_p
             L.ccl_set_option.argtypes = [i32, ctypes.c_longlong]
             L.ccl_set_option.restype = i32
+            L.ccl_stage_times.argtypes = [vp, i32, vp]
+            L.ccl_stage_times.restype = i32
+            L.ccl_stage_name.argtypes = [i32]
+            L.ccl_stage_name.restype = ctypes.c_char_p
+            L.ccl_kernel_launches.argtypes = []
+            L.ccl_kernel_launches.restype = ctypes.c_longlong
             L.ccl_version.argtypes = []
             L.ccl_version.restype = i32
             _lib = L
@@ -104,6 +112,24 @@ def ccl_status_string(status):
 
 def ccl_set_option(option, value):
     return lib().ccl_set_option(option, value)
+
+
+def ccl_stage_times(max_stages=8):
+    """Returns (list of summed ms per stage, number of calls recorded)."""
+    arr = (ctypes.c_double * max_stages)()
+    n = ctypes.c_int(0)
+    k = lib().ccl_stage_times(arr, max_stages, ctypes.byref(n))
+    if k < 0:
+        raise CCLError(-k, "ccl_stage_times")
+    return [arr[i] for i in range(min(k, max_stages))], n.value
+
+
+def ccl_stage_name(stage):
+    return lib().ccl_stage_name(stage).decode()
+
+
+def ccl_kernel_launches():
+    return lib().ccl_kernel_launches()
 
 
 def ccl_version():

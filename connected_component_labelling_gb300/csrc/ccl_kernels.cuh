@@ -1,0 +1,724 @@
+// ccl_kernels.cuh -- device code of the labelling library (sm_103a).
+//
+// The four stages of "every-colour" (blogs.fablnx.com) ch. 05 -- Start,
+// Connect, Collapse, Number -- as five kernels over 256 x TH pixel tiles:
+//
+//   k_tile_local  Start + Connect + Collapse inside one tile, in shared
+//                 memory.  A lane owns 8 consecutive pixels of a row; runs of
+//                 equal colour are found with a warp scan of run starts
+//                 (ch. 08 switch 1, the warp finds the runs) so that a run is
+//                 one union-find node.  Joins go to the row above first and
+//                 skip what the left neighbour already joins (ch. 08 "First,
+//                 the order of the joins" and switch 2, the Wu-Otoo-Suzuki
+//                 scan mask); walks halve paths with the same atomic minimum
+//                 (switch 3).  Output: a 2-byte tile-local leader per pixel,
+//                 a leader bitmap, a leader count per 256-pixel chunk of a
+//                 row, and a global parent slot (its own raster index) for
+//                 every leader whose region touches the tile border.
+//   k_seams       Connect across tile seams: the joins of the same rule whose
+//                 partner is in another tile, united in the global parent
+//                 array with atomicMin and retry (ch. 06 Fig. 10;
+//                 bendabir.com, "Unions are parallel").  A leader that is
+//                 re-pointed leaves the bitmap and its chunk count.
+//   k_compress    Collapse for the border leaders: each points straight at
+//                 its final leader.
+//   k_scan_*      Number, first half: exclusive prefix sum of chunk counts
+//                 (ch. 08 switch 5; ch. 12, a prefix sum inside Number).
+//   k_number      Number, second half: a leader's label is 1 + the number of
+//                 leaders before it in raster order; every pixel takes its
+//                 tile-local leader's label.
+//
+// Leaders are always the smallest raster index of their set (ch. 04: the
+// larger leader points at the smaller one), so the labels come out in the
+// raster order of each region's first pixel.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace ccl_dev {
+
+constexpr int TW = 256;             // tile width == numbering chunk width
+constexpr int LOG_TW = 8;
+constexpr int TH = 16;              // tile height
+constexpr int TILE = TW * TH;
+constexpr int NT = 256;             // threads per block
+constexpr int NWARPS = NT / 32;
+constexpr int RPW = TH / NWARPS;    // tile rows per warp
+constexpr int PX = TW / 32;         // consecutive pixels per lane
+constexpr int CHUNK = 256;          // pixels of a row counted together
+constexpr int SCAN_ITEMS = 16;
+constexpr int SCAN_BLOCK = NT * SCAN_ITEMS;
+constexpr uint16_t LBG = 0xFFFF;    // background in the tile-local leader map
+constexpr unsigned FULL = 0xffffffffu;
+static_assert(PX == 8, "a lane owns 8 pixels");
+static_assert(TH % NWARPS == 0, "whole rows per warp");
+
+constexpr int FLAG_WALK_CAP = 1;    // a union-find walk or retry loop hit its cap
+constexpr int FLAG_INTERNAL = 2;    // an invariant of the numbering pass failed
+
+struct Geom {
+  int H, W;
+  int tilesX, tilesY;
+  int WPR;                      // bitmap words per row = ceil(W / 32)
+  int CPR;                      // chunks per row       = ceil(W / 256)
+  long long HW;                 // pixels per image
+  long long tilesPerImage;
+  unsigned long long wmagic;    // exact d / W for 0 <= d < 2^31: (d * wmagic) >> wshift
+  int wshift;
+  int vec_img;                  // image rows allow 8-pixel vector loads
+  int vec_out;                  // leader-map and label rows allow vector access
+};
+
+struct TileCoord {
+  int b, tx, y0, x0, th, tw;
+};
+
+__device__ __forceinline__ TileCoord tile_coord(const Geom& g) {
+  TileCoord t;
+  const long long tile = blockIdx.x;
+  t.b = (int)(tile / g.tilesPerImage);
+  const int rest = (int)(tile - (long long)t.b * g.tilesPerImage);
+  const int ty = rest / g.tilesX;
+  t.tx = rest - ty * g.tilesX;
+  t.y0 = ty * TH;
+  t.x0 = t.tx * TW;
+  t.th = min(TH, g.H - t.y0);
+  t.tw = min(TW, g.W - t.x0);
+  return t;
+}
+
+__device__ __forceinline__ int div_w(int d, const Geom& g) {
+  return (int)(((unsigned long long)(unsigned)d * g.wmagic) >> g.wshift);
+}
+
+__device__ __forceinline__ void raise_flag(int* status, int f) { atomicOr(status, f); }
+
+// ---------------------------------------------------------------- pixel I/O
+// Eight consecutive pixels, widened to 32 bits.
+
+template <typename T>
+__device__ __forceinline__ void load8(const T* p, bool vec, int n, uint32_t c[PX]);
+
+template <>
+__device__ __forceinline__ void load8<uint8_t>(const uint8_t* p, bool vec, int n, uint32_t c[PX]) {
+  if (vec) {
+    const uint2 v = __ldg(reinterpret_cast<const uint2*>(p));
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      c[j] = (v.x >> (8 * j)) & 0xFFu;
+      c[j + 4] = (v.y >> (8 * j)) & 0xFFu;
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < PX; ++j) c[j] = j < n ? (uint32_t)__ldg(p + j) : 0u;
+  }
+}
+
+template <>
+__device__ __forceinline__ void load8<uint16_t>(const uint16_t* p, bool vec, int n, uint32_t c[PX]) {
+  if (vec) {
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(p));
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      c[2 * j] = w[j] & 0xFFFFu;
+      c[2 * j + 1] = w[j] >> 16;
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < PX; ++j) c[j] = j < n ? (uint32_t)__ldg(p + j) : 0u;
+  }
+}
+
+template <>
+__device__ __forceinline__ void load8<uint32_t>(const uint32_t* p, bool vec, int n, uint32_t c[PX]) {
+  if (vec) {
+    const uint4 a = __ldg(reinterpret_cast<const uint4*>(p));
+    const uint4 b = __ldg(reinterpret_cast<const uint4*>(p) + 1);
+    c[0] = a.x; c[1] = a.y; c[2] = a.z; c[3] = a.w;
+    c[4] = b.x; c[5] = b.y; c[6] = b.z; c[7] = b.w;
+  } else {
+#pragma unroll
+    for (int j = 0; j < PX; ++j) c[j] = j < n ? __ldg(p + j) : 0u;
+  }
+}
+
+// shared-memory copies of a lane's 8 pixels (16-byte aligned addresses)
+template <typename T>
+__device__ __forceinline__ void st8s(T* s, const uint32_t c[PX]) {
+#pragma unroll
+  for (int j = 0; j < PX; ++j) s[j] = (T)c[j];
+}
+template <>
+__device__ __forceinline__ void st8s<uint32_t>(uint32_t* s, const uint32_t c[PX]) {
+  reinterpret_cast<uint4*>(s)[0] = make_uint4(c[0], c[1], c[2], c[3]);
+  reinterpret_cast<uint4*>(s)[1] = make_uint4(c[4], c[5], c[6], c[7]);
+}
+template <typename T>
+__device__ __forceinline__ void ld8s(const T* s, uint32_t c[PX]) {
+#pragma unroll
+  for (int j = 0; j < PX; ++j) c[j] = s[j];
+}
+template <>
+__device__ __forceinline__ void ld8s<uint32_t>(const uint32_t* s, uint32_t c[PX]) {
+  const uint4 a = reinterpret_cast<const uint4*>(s)[0];
+  const uint4 b = reinterpret_cast<const uint4*>(s)[1];
+  c[0] = a.x; c[1] = a.y; c[2] = a.z; c[3] = a.w;
+  c[4] = b.x; c[5] = b.y; c[6] = b.z; c[7] = b.w;
+}
+
+// ------------------------------------------------------------ shared memory
+// Union-find over tile-local indices r * TW + x.  Reads go through a
+// volatile pointer so every step sees other threads' links.
+
+__device__ __forceinline__ int find_s(volatile int* par, int x, int cap, int* status) {
+  for (int s = 0; s < cap; ++s) {
+    const int p = par[x];
+    if (p == x) return x;
+    const int gp = par[p];
+    if (gp == p) return p;
+    atomicMin((int*)&par[x], gp);   // path halving: an arrow only ever moves down
+    x = gp;
+  }
+  raise_flag(status, FLAG_WALK_CAP);
+  return x;
+}
+
+__device__ __forceinline__ void union_s(volatile int* par, int a, int b, int cap, int* status) {
+  for (int s = 0; s < cap; ++s) {
+    a = find_s(par, a, cap, status);
+    b = find_s(par, b, cap, status);
+    if (a == b) return;
+    if (a > b) { const int t = a; a = b; b = t; }
+    const int old = atomicMin((int*)&par[b], a);   // larger leader under smaller
+    if (old == b) return;
+    b = old;                                         // someone got there first
+  }
+  raise_flag(status, FLAG_WALK_CAP);
+}
+
+// ------------------------------------------------------------ global memory
+// Union-find over image raster indices.  Only leaders' slots are touched:
+// every walk starts at a tile-local leader and every node after that is a
+// leader too.
+
+// Every loaded arrow is range-checked before it is followed: if a capped
+// walk in an earlier stage left a pixel pointing at a non-leader, whose slot
+// was never written, the walk stops with -1 instead of leaving the image.
+__device__ __forceinline__ int find_g(int* P, int x, int n, int cap, int* status) {
+  for (int s = 0; s < cap; ++s) {
+    const int p = __ldcg(P + x);
+    if (p == x) return x;
+    if ((unsigned)p >= (unsigned)n) {
+      raise_flag(status, FLAG_INTERNAL);
+      return -1;
+    }
+    const int gp = __ldcg(P + p);
+    if (gp == p) return p;
+    if ((unsigned)gp >= (unsigned)n) {
+      raise_flag(status, FLAG_INTERNAL);
+      return -1;
+    }
+    atomicMin(P + x, gp);
+    x = gp;
+  }
+  raise_flag(status, FLAG_WALK_CAP);
+  return -1;
+}
+
+__device__ __forceinline__ void drop_leader(int b, uint32_t* bm, uint32_t* cnt, const Geom& g) {
+  const int by = div_w(b, g);
+  const int bx = b - by * g.W;
+  atomicAnd(bm + (size_t)by * g.WPR + (bx >> 5), ~(1u << (bx & 31)));
+  atomicSub(cnt + (size_t)by * g.CPR + (bx >> LOG_TW), 1u);
+}
+
+__device__ __forceinline__ void union_g(int* P, int a, int b, uint32_t* bm, uint32_t* cnt,
+                                        const Geom& g, int cap, int* status) {
+  const int n = (int)g.HW;
+  for (int s = 0; s < cap; ++s) {
+    a = find_g(P, a, n, cap, status);
+    b = find_g(P, b, n, cap, status);
+    if (a < 0 || b < 0 || a == b) return;
+    if (a > b) { const int t = a; a = b; b = t; }
+    const int old = atomicMin(P + b, a);
+    if (old == b) {            // b stopped being a leader, exactly once
+      drop_leader(b, bm, cnt, g);
+      return;
+    }
+    b = old;
+  }
+  raise_flag(status, FLAG_WALK_CAP);
+}
+
+// image raster index of the tile-local leader of pixel (y, x), -1 for background
+__device__ __forceinline__ int leader_of(const uint16_t* Li, int y, int x, const Geom& g) {
+  const uint16_t l = Li[(long long)y * g.W + x];
+  if (l >= TILE) return -1;   // background (LBG)
+  const int ly = (y & ~(TH - 1)) + (l >> LOG_TW), lx = (x & ~(TW - 1)) + (l & (TW - 1));
+  if (ly >= g.H || lx >= g.W) return -1;   // only a corrupted map can get here
+  return ly * g.W + lx;
+}
+
+__device__ __forceinline__ int warp_sum(int v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(FULL, v, o);
+  return v;
+}
+
+// ------------------------------------------------------------------ kernels
+
+template <typename T, int CONN, bool BIN>
+__global__ void __launch_bounds__(NT) k_tile_local(const T* __restrict__ img, uint16_t* __restrict__ L16,
+                                                   int32_t* __restrict__ P, uint32_t* __restrict__ bm,
+                                                   uint32_t* __restrict__ cnt, Geom g, int cap,
+                                                   int* status) {
+  __shared__ __align__(16) T col[TILE];
+  __shared__ __align__(16) int par[TILE];
+  __shared__ __align__(16) uint8_t mark[TILE];
+  const TileCoord t = tile_coord(g);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, xl = lane * PX;
+  const long long ioff = (long long)t.b * g.HW;
+  const T* im = img + ioff;
+  uint16_t* Li = L16 + ioff;
+  int32_t* Pi = P + ioff;
+  uint32_t* bmi = bm + (long long)t.b * g.H * g.WPR;
+  uint32_t* cnti = cnt + (long long)t.b * g.H * g.CPR;
+  for (int i = threadIdx.x * 16; i < TILE; i += NT * 16)
+    *reinterpret_cast<uint4*>(mark + i) = make_uint4(0, 0, 0, 0);
+  const int nval = max(0, min(PX, t.tw - xl));
+  const unsigned vmask = (1u << nval) - 1u;
+  const bool vec = g.vec_img && nval == PX;
+  unsigned fgm[RPW], eqm[RPW];
+
+  // ---- Start: each pixel points at the first pixel of its run in the row
+#pragma unroll
+  for (int k = 0; k < RPW; ++k) {
+    const int r = warp + k * NWARPS;
+    fgm[k] = 0;
+    eqm[k] = 0;
+    if (r >= t.th) continue;   // warp-uniform
+    uint32_t c[PX];
+    load8<T>(im + (long long)(t.y0 + r) * g.W + t.x0 + xl, vec, nval, c);
+    unsigned fg = vmask;
+    if (BIN) {
+#pragma unroll
+      for (int j = 0; j < PX; ++j)
+        if (c[j] == 0) fg &= ~(1u << j);
+    }
+    const uint32_t cl = __shfl_up_sync(FULL, c[PX - 1], 1);
+    const unsigned fgl = __shfl_up_sync(FULL, fg, 1);
+    unsigned eq = (lane > 0 && (fg & 1u) && ((fgl >> (PX - 1)) & 1u) && c[0] == cl) ? 1u : 0u;
+#pragma unroll
+    for (int j = 1; j < PX; ++j)
+      if (((fg >> j) & (fg >> (j - 1)) & 1u) && c[j] == c[j - 1]) eq |= 1u << j;
+    const unsigned starts = fg & ~eq;
+    int last = starts ? xl + 31 - __clz(starts) : -1;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(FULL, last, o);
+      if (lane >= o) last = max(last, y);
+    }
+    int before = __shfl_up_sync(FULL, last, 1);
+    if (lane == 0) before = -1;
+    int pv[PX];
+#pragma unroll
+    for (int j = 0; j < PX; ++j) {
+      const unsigned m = starts & ((2u << j) - 1u);
+      const int s = m ? xl + 31 - __clz(m) : before;
+      pv[j] = ((fg >> j) & 1u) ? r * TW + s : -1;
+    }
+    int4* pp = reinterpret_cast<int4*>(par + r * TW + xl);
+    pp[0] = make_int4(pv[0], pv[1], pv[2], pv[3]);
+    pp[1] = make_int4(pv[4], pv[5], pv[6], pv[7]);
+    st8s<T>(col + r * TW + xl, c);
+    fgm[k] = fg;
+    eqm[k] = eq;
+  }
+  __syncthreads();
+
+  // ---- Connect inside the tile: row above first; a pixel whose left
+  // neighbour has its colour leaves up-left and up to that neighbour.
+  // Neighbours outside the tile count as absent here (k_seams joins them).
+#pragma unroll
+  for (int k = 0; k < RPW; ++k) {
+    const int r = warp + k * NWARPS;
+    if (r >= t.th || r == 0) continue;   // warp-uniform
+    uint32_t c[PX], u[PX];
+    ld8s<T>(col + r * TW + xl, c);
+    ld8s<T>(col + (r - 1) * TW + xl, u);
+    const uint32_t uL = __shfl_up_sync(FULL, u[PX - 1], 1);
+    const uint32_t uR = __shfl_down_sync(FULL, u[0], 1);
+    const unsigned fg = fgm[k], eq = eqm[k];
+    if (!fg) continue;
+    const bool hasL = lane > 0;
+    const bool hasR = lane < 31 && xl + PX < t.tw;
+    const int i0 = r * TW + xl;
+#pragma unroll
+    for (int j = 0; j < PX; ++j) {
+      if (!((fg >> j) & 1u)) continue;
+      const uint32_t cj = c[j];
+      const bool eqL = (eq >> j) & 1u;
+      const bool eqU = cj == u[j];
+      const bool eqUL = j > 0 ? cj == u[j - 1] : (hasL && cj == uL);
+      if (CONN == 8) {
+        const bool eqUR = j < PX - 1 ? (((vmask >> (j + 1)) & 1u) && cj == u[j + 1]) : (hasR && cj == uR);
+        if (eqU && !eqL) union_s(par, i0 + j, i0 + j - TW, cap, status);
+        if (eqUL && !eqU && !eqL) union_s(par, i0 + j, i0 + j - TW - 1, cap, status);
+        if (eqUR && !eqU) union_s(par, i0 + j, i0 + j - TW + 1, cap, status);
+      } else {
+        if (eqU && !(eqL && eqUL)) union_s(par, i0 + j, i0 + j - TW, cap, status);
+      }
+    }
+  }
+  __syncthreads();
+
+  // ---- Collapse inside the tile: one walk per run; write the leader map,
+  // the leader bitmap and the chunk counts; mark leaders on the border
+  unsigned rootm[RPW];
+#pragma unroll
+  for (int k = 0; k < RPW; ++k) {
+    const int r = warp + k * NWARPS;
+    rootm[k] = 0;
+    if (r >= t.th) continue;   // warp-uniform
+    const unsigned fg = fgm[k], starts = fg & ~eqm[k];
+    const int i0 = r * TW + xl;
+    const bool edgeRow = r == 0 || r == t.th - 1;
+    uint32_t lv[PX];
+    unsigned rm = 0;
+    int cur = 0;
+#pragma unroll
+    for (int j = 0; j < PX; ++j) {
+      lv[j] = LBG;
+      if (!((fg >> j) & 1u)) continue;
+      if (j == 0 || ((starts >> j) & 1u)) cur = find_s(par, i0 + j, cap, status);
+      lv[j] = (uint32_t)cur;
+      if (cur == i0 + j) rm |= 1u << j;
+      const int x = xl + j;
+      if (edgeRow || x == 0 || x == t.tw - 1) mark[cur] = 1;
+    }
+    uint16_t* lrow = Li + (long long)(t.y0 + r) * g.W + t.x0 + xl;
+    if (g.vec_out && nval == PX) {
+      *reinterpret_cast<uint4*>(lrow) = make_uint4(lv[0] | (lv[1] << 16), lv[2] | (lv[3] << 16),
+                                                   lv[4] | (lv[5] << 16), lv[6] | (lv[7] << 16));
+    } else {
+#pragma unroll
+      for (int j = 0; j < PX; ++j)
+        if (j < nval) lrow[j] = (uint16_t)lv[j];
+    }
+    const unsigned b1 = __shfl_down_sync(FULL, rm, 1);
+    const unsigned b2 = __shfl_down_sync(FULL, rm, 2);
+    const unsigned b3 = __shfl_down_sync(FULL, rm, 3);
+    if ((lane & 3) == 0 && xl < t.tw)
+      bmi[(long long)(t.y0 + r) * g.WPR + ((t.x0 + xl) >> 5)] = rm | (b1 << 8) | (b2 << 16) | (b3 << 24);
+    const int n = warp_sum(__popc(rm));
+    if (lane == 0) cnti[(long long)(t.y0 + r) * g.CPR + t.tx] = (uint32_t)n;
+    rootm[k] = rm;
+  }
+  __syncthreads();
+
+  // ---- global parent slots for leaders whose region touches the border
+#pragma unroll
+  for (int k = 0; k < RPW; ++k) {
+    const int r = warp + k * NWARPS;
+    if (r >= t.th || !rootm[k]) continue;
+#pragma unroll
+    for (int j = 0; j < PX; ++j) {
+      if (((rootm[k] >> j) & 1u) && mark[r * TW + xl + j]) {
+        const int gi = (t.y0 + r) * g.W + t.x0 + xl + j;
+        Pi[gi] = gi;
+      }
+    }
+  }
+}
+
+// The joins of pixel (y, x) -- the same rule as inside a tile, on the true
+// neighbourhood -- whose partner lies outside the pixel's tile.
+template <typename T, int CONN, bool BIN>
+__device__ __forceinline__ void seam_joins(const T* __restrict__ im, const uint16_t* __restrict__ Li,
+                                           int32_t* P, uint32_t* bm, uint32_t* cnt, const Geom& g,
+                                           int y, int x, int y0, int x0, int cap, int* status) {
+  const long long row = (long long)y * g.W;
+  const T c = im[row + x];
+  if (BIN && c == 0) return;
+  const bool hasU = y > 0, hasL = x > 0;
+  const bool eqL = hasL && im[row + x - 1] == c;
+  const bool eqU = hasU && im[row - g.W + x] == c;
+  const bool eqUL = hasU && hasL && im[row - g.W + x - 1] == c;
+  const bool eqUR = (CONN == 8) && hasU && x + 1 < g.W && im[row - g.W + x + 1] == c;
+  int a = -1;
+  auto join = [&](int qy, int qx) {
+    if (qy >= y0 && qx >= x0 && qx < x0 + TW) return;   // inside the tile
+    if (a < 0) a = leader_of(Li, y, x, g);
+    const int bq = leader_of(Li, qy, qx, g);
+    union_g(P, a, bq, bm, cnt, g, cap, status);
+  };
+  if (CONN == 8) {
+    if (eqU && !eqL) join(y - 1, x);
+    if (eqUL && !eqU && !eqL) join(y - 1, x - 1);
+    if (eqUR && !eqU) join(y - 1, x + 1);
+  } else {
+    if (eqU && !(eqL && eqUL)) join(y - 1, x);
+  }
+  if (eqL) join(y, x - 1);
+}
+
+template <typename T, int CONN, bool BIN>
+__global__ void __launch_bounds__(NT) k_seams(const T* __restrict__ img, const uint16_t* __restrict__ L16,
+                                              int32_t* P, uint32_t* bm, uint32_t* cnt, Geom g, int cap,
+                                              int* status) {
+  const TileCoord t = tile_coord(g);
+  const long long ioff = (long long)t.b * g.HW;
+  const T* im = img + ioff;
+  const uint16_t* Li = L16 + ioff;
+  int32_t* Pi = P + ioff;
+  uint32_t* bmi = bm + (long long)t.b * g.H * g.WPR;
+  uint32_t* cnti = cnt + (long long)t.b * g.H * g.CPR;
+  const int nTop = t.tw, nSide = t.th - 1;
+  for (int k = threadIdx.x; k < nTop + 2 * nSide; k += NT) {
+    int y, x;
+    if (k < nTop) { y = t.y0; x = t.x0 + k; }
+    else if (k < nTop + nSide) { y = t.y0 + 1 + (k - nTop); x = t.x0; }
+    else { y = t.y0 + 1 + (k - nTop - nSide); x = t.x0 + t.tw - 1; }
+    seam_joins<T, CONN, BIN>(im, Li, Pi, bmi, cnti, g, y, x, t.y0, t.x0, cap, status);
+  }
+}
+
+// Collapse for the leaders that took part in seam joins: every such
+// leader's tile region touches the tile border, so walking from the border
+// pixels reaches all of them.
+__global__ void __launch_bounds__(NT) k_compress(const uint16_t* __restrict__ L16, int32_t* P, Geom g,
+                                                 int cap, int* status) {
+  const TileCoord t = tile_coord(g);
+  const long long ioff = (long long)t.b * g.HW;
+  const uint16_t* Li = L16 + ioff;
+  int32_t* Pi = P + ioff;
+  const int n = 2 * t.tw + 2 * t.th;
+  for (int k = threadIdx.x; k < n; k += NT) {
+    int y, x;
+    if (k < t.tw) { y = t.y0; x = t.x0 + k; }
+    else if (k < 2 * t.tw) { y = t.y0 + t.th - 1; x = t.x0 + (k - t.tw); }
+    else if (k < 2 * t.tw + t.th) { y = t.y0 + (k - 2 * t.tw); x = t.x0; }
+    else { y = t.y0 + (k - 2 * t.tw - t.th); x = t.x0 + t.tw - 1; }
+    const int r = leader_of(Li, y, x, g);
+    if (r < 0) continue;
+    const int root = find_g(Pi, r, (int)g.HW, cap, status);
+    if (root >= 0 && root != r) atomicMin(Pi + r, root);
+  }
+}
+
+// ---- exclusive prefix sum of the chunk counts (three passes, no waits)
+
+__device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* total) {
+  __shared__ uint32_t warp_sums[NWARPS];
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  uint32_t inc = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(FULL, inc, o);
+    if (lane >= o) inc += y;
+  }
+  if (lane == 31) warp_sums[wid] = inc;
+  __syncthreads();
+  if (wid == 0) {
+    const uint32_t s = lane < NWARPS ? warp_sums[lane] : 0;
+    uint32_t si = s;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(FULL, si, o);
+      if (lane >= o) si += y;
+    }
+    if (lane < NWARPS) warp_sums[lane] = si - s;
+    if (lane == NWARPS - 1) *total = si;
+  }
+  __syncthreads();
+  const uint32_t res = inc - v + warp_sums[wid];
+  __syncthreads();
+  return res;
+}
+
+__global__ void __launch_bounds__(NT) k_scan_reduce(const uint32_t* __restrict__ cnt, long long n,
+                                                    uint32_t* __restrict__ bsum) {
+  __shared__ uint32_t tot;
+  const long long base = (long long)blockIdx.x * SCAN_BLOCK + (long long)threadIdx.x * SCAN_ITEMS;
+  uint32_t s = 0;
+#pragma unroll
+  for (int k = 0; k < SCAN_ITEMS; ++k)
+    if (base + k < n) s += cnt[base + k];
+  block_exclusive_scan(s, &tot);
+  if (threadIdx.x == 0) bsum[blockIdx.x] = tot;
+}
+
+// one block: exclusive scan of the block sums, grand total at bsum[nb]
+__global__ void __launch_bounds__(NT) k_scan_top(uint32_t* bsum, int nb) {
+  __shared__ uint32_t tot;
+  uint32_t carry = 0;
+  for (int base = 0; base < nb; base += NT) {
+    const int i = base + threadIdx.x;
+    const uint32_t v = i < nb ? bsum[i] : 0;
+    const uint32_t ex = block_exclusive_scan(v, &tot);
+    if (i < nb) bsum[i] = carry + ex;
+    carry += tot;
+  }
+  if (threadIdx.x == 0) bsum[nb] = carry;
+}
+
+__global__ void __launch_bounds__(NT) k_scan_down(uint32_t* cnt, long long n, const uint32_t* bsum) {
+  __shared__ uint32_t tot;
+  const long long base = (long long)blockIdx.x * SCAN_BLOCK + (long long)threadIdx.x * SCAN_ITEMS;
+  uint32_t v[SCAN_ITEMS];
+  uint32_t s = 0;
+#pragma unroll
+  for (int k = 0; k < SCAN_ITEMS; ++k) {
+    v[k] = base + k < n ? cnt[base + k] : 0;
+    s += v[k];
+  }
+  uint32_t run = block_exclusive_scan(s, &tot) + bsum[blockIdx.x];
+#pragma unroll
+  for (int k = 0; k < SCAN_ITEMS; ++k) {
+    if (base + k < n) cnt[base + k] = run;
+    run += v[k];
+  }
+  if (blockIdx.x == gridDim.x - 1 && threadIdx.x == 0) cnt[n] = bsum[gridDim.x];
+}
+
+__global__ void k_region_counts(const uint32_t* off, long long chunksPerImage, int batch,
+                                int32_t* n_out) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b < batch)
+    n_out[b] = (int32_t)(off[(long long)(b + 1) * chunksPerImage] - off[(long long)b * chunksPerImage]);
+}
+
+// label of leader gidx: 1 + leaders before it in raster order within its image
+__device__ __forceinline__ int number_of(int gidx, const uint32_t* bmi, const uint32_t* offi,
+                                         uint32_t base0, const Geom& g, int* status) {
+  if (gidx < 0 || (long long)gidx >= g.HW) {
+    raise_flag(status, FLAG_INTERNAL);
+    return 0;
+  }
+  const int gy = div_w(gidx, g), gx = gidx - gy * g.W;
+  const long long w0 = (long long)gy * g.WPR + ((gx >> LOG_TW) << 3);
+  const long long wg = (long long)gy * g.WPR + (gx >> 5);
+  uint32_t s = 0;
+  for (long long w = w0; w < wg; ++w) s += __popc(bmi[w]);
+  const uint32_t word = bmi[wg];
+  if (!((word >> (gx & 31)) & 1u)) raise_flag(status, FLAG_INTERNAL);
+  s += __popc(word & ((1u << (gx & 31)) - 1u));
+  return (int)(offi[(long long)gy * g.CPR + (gx >> LOG_TW)] - base0 + s + 1u);
+}
+
+// Number: labels of the tile's leaders from the bitmap and the chunk offsets,
+// then every pixel takes its tile-local leader's label.  The labels buffer
+// holds the global parent slots of border leaders until this kernel
+// overwrites them; a tile reads only its own slots, before writing.
+__global__ void __launch_bounds__(NT) k_number(const uint16_t* __restrict__ L16, int32_t* labels,
+                                               const uint32_t* __restrict__ bm,
+                                               const uint32_t* __restrict__ off, Geom g, int* status) {
+  __shared__ __align__(16) int lab[TILE];
+  const TileCoord t = tile_coord(g);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, xl = lane * PX;
+  const long long ioff = (long long)t.b * g.HW;
+  const uint16_t* Li = L16 + ioff;
+  int32_t* Pi = labels + ioff;
+  const uint32_t* bmi = bm + (long long)t.b * g.H * g.WPR;
+  const uint32_t* offi = off + (long long)t.b * g.H * g.CPR;
+  const uint32_t base0 = offi[0];
+  const int nval = max(0, min(PX, t.tw - xl));
+  const bool vec = g.vec_out && nval == PX;
+  uint32_t lw[RPW][PX / 2];   // the lane's 8 leader-map entries per row, two per word
+
+#pragma unroll
+  for (int k = 0; k < RPW; ++k) {
+    const int r = warp + k * NWARPS;
+#pragma unroll
+    for (int q = 0; q < PX / 2; ++q) lw[k][q] = 0xFFFFFFFFu;
+    if (r >= t.th) continue;   // warp-uniform
+    const uint16_t* lrow = Li + (long long)(t.y0 + r) * g.W + t.x0 + xl;
+    if (vec) {
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(lrow));
+      lw[k][0] = v.x; lw[k][1] = v.y; lw[k][2] = v.z; lw[k][3] = v.w;
+    } else {
+#pragma unroll
+      for (int j = 0; j < PX; ++j) {
+        const uint32_t l = j < nval ? (uint32_t)lrow[j] : 0xFFFFu;
+        lw[k][j >> 1] = (j & 1) ? ((lw[k][j >> 1] & 0xFFFFu) | (l << 16))
+                                : ((lw[k][j >> 1] & 0xFFFF0000u) | l);
+      }
+    }
+    // leaders of this row: rank within the row from the bitmap
+    // word w of the row segment belongs to lanes 4w..4w+3; lane 4w counts it
+    const uint32_t w = xl < t.tw ? bmi[(long long)(t.y0 + r) * g.WPR + ((t.x0 + xl) >> 5)] : 0u;
+    const uint32_t mine = ((lane & 3) == 0) ? __popc(w) : 0u;
+    uint32_t inc = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(FULL, inc, o);
+      if (lane >= o) inc += y;
+    }
+    // leaders in the words before this lane's word
+    const uint32_t pre = __shfl_sync(FULL, inc - mine, lane & ~3);
+    const uint32_t o = offi[(long long)(t.y0 + r) * g.CPR + t.tx] - base0;
+    const int i0 = r * TW + xl;
+#pragma unroll
+    for (int j = 0; j < PX; ++j) {
+      const int l = (int)((lw[k][j >> 1] >> (16 * (j & 1))) & 0xFFFFu);
+      if (l != i0 + j) continue;   // not a leader
+      const int bit = (xl + j) & 31;
+      if ((w >> bit) & 1u) {
+        lab[i0 + j] = (int)(o + pre + __popc(w & ((1u << bit) - 1u)) + 1u);
+      } else {
+        // re-pointed across a seam: k_compress left the final leader here
+        const int gi = (t.y0 + r) * g.W + t.x0 + xl + j;
+        const int gg = Pi[gi];
+        const int gy = div_w(gg, g), gx = gg - gy * g.W;
+        if (gg >= 0 && gy >= t.y0 && gy < t.y0 + t.th && gx >= t.x0 && gx < t.x0 + t.tw)
+          lab[i0 + j] = -1 - (((gy - t.y0) << LOG_TW) + (gx - t.x0));
+        else
+          lab[i0 + j] = number_of(gg, bmi, offi, base0, g, status);
+      }
+    }
+  }
+  __syncthreads();
+  // leaders whose final leader is in this tile take its label
+#pragma unroll
+  for (int k = 0; k < RPW; ++k) {
+    const int r = warp + k * NWARPS;
+    if (r >= t.th) continue;
+    const int i0 = r * TW + xl;
+#pragma unroll
+    for (int j = 0; j < PX; ++j) {
+      const int l = (int)((lw[k][j >> 1] >> (16 * (j & 1))) & 0xFFFFu);
+      if (l != i0 + j) continue;
+      const int v = lab[i0 + j];
+      if (v < 0) {
+        const int w = lab[-1 - v];
+        if (w <= 0) raise_flag(status, FLAG_INTERNAL);
+        lab[i0 + j] = w > 0 ? w : 0;
+      }
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int k = 0; k < RPW; ++k) {
+    const int r = warp + k * NWARPS;
+    if (r >= t.th) continue;
+    int out[PX];
+#pragma unroll
+    for (int j = 0; j < PX; ++j) {
+      const int l = (int)((lw[k][j >> 1] >> (16 * (j & 1))) & 0xFFFFu);
+      out[j] = (l == LBG || l >= TILE) ? 0 : lab[l];
+    }
+    int32_t* orow = Pi + (long long)(t.y0 + r) * g.W + t.x0 + xl;
+    if (vec) {
+      reinterpret_cast<int4*>(orow)[0] = make_int4(out[0], out[1], out[2], out[3]);
+      reinterpret_cast<int4*>(orow)[1] = make_int4(out[4], out[5], out[6], out[7]);
+    } else {
+#pragma unroll
+      for (int j = 0; j < PX; ++j)
+        if (j < nval) orow[j] = out[j];
+    }
+  }
+}
+
+}  // namespace ccl_dev

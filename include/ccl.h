@@ -126,10 +126,28 @@ const char* ccl_status_string(int status);
  *                     (value <= 0 restores the default, the number of pixels
  *                     the walk can visit); lowering it lets a test make the
  *                     device report CCL_ERR_DEVICE_LIMIT without any hang.
+ *   CCL_OPT_STAGE_EVENTS  non-zero: record per-stage CUDA events in every
+ *                     call (see ccl_stage_times); 0: stop recording.
  * Returns CCL_OK or CCL_ERR_INVALID_ARG for an unknown option.
  */
-enum { CCL_OPT_WALK_CAP = 1 };
+enum { CCL_OPT_WALK_CAP = 1, CCL_OPT_STAGE_EVENTS = 2 };
 int ccl_set_option(int option, long long value);
+
+/*
+ * Per-stage device timing.  While option CCL_OPT_STAGE_EVENTS is non-zero
+ * every labelling call records a CUDA event on its own stream before its
+ * first kernel and after each stage (the stages are named by
+ * ccl_stage_name: 0 tile_local, 1 seams, 2 compress, 3 scan, 4 number).
+ * ccl_stage_times waits for those events, writes the summed milliseconds of
+ * each stage over all recorded calls into ms_sum[0..max_stages) and the call
+ * count into *n_calls (either pointer may be NULL), forgets the recorded
+ * calls and returns the number of stages (or a negative ccl_status).
+ */
+int ccl_stage_times(double* ms_sum, int max_stages, int* n_calls);
+const char* ccl_stage_name(int stage);
+
+/* Number of CUDA kernels this library has launched in this process. */
+long long ccl_kernel_launches(void);
 
 /* Library version, as major*10000 + minor*100 + patch. */
 int ccl_version(void);

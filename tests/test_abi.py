@@ -27,7 +27,8 @@ def declared_functions():
 def test_header_declares_the_entry_points():
     names = declared_functions()
     for n in ("ccl_label", "ccl_label_ws", "ccl_workspace_bytes", "ccl_label_host",
-              "ccl_last_status", "ccl_status_string", "ccl_set_option", "ccl_version"):
+              "ccl_last_status", "ccl_status_string", "ccl_set_option", "ccl_stage_times",
+              "ccl_stage_name", "ccl_kernel_launches", "ccl_version"):
         assert n in names
     assert sorted(ccl.EXPORTED) == names
 
@@ -56,8 +57,9 @@ def test_workspace_bytes(lib):
     a = ccl.ccl_workspace_bytes(1, 1024, 1024, 4, 8, 0)
     b = ccl.ccl_workspace_bytes(2, 1024, 1024, 4, 8, 0)
     assert 0 < a < b
-    # bitmap (1 bit/px) + one count per 256 px, rounded: far below the labels
-    assert a < 1024 * 1024 // 4
+    # 2-byte tile-local leader map + bitmap (1 bit/px) + one count per 256 px
+    px = 1024 * 1024
+    assert 2 * px + px // 8 <= a < 2 * px + px // 8 + px // 32
     assert a % 256 == 0
 
 
@@ -96,7 +98,17 @@ def test_workspace_checks_on_host(lib):
     assert ccl.ccl_label_ws(*args, None, need, None) == ccl.CCL_ERR_INVALID_ARG
 
 
+def test_stage_names_and_counter(lib):
+    assert [ccl.ccl_stage_name(k) for k in range(5)] == [
+        "tile_local", "seams", "compress", "scan", "number"]
+    assert ccl.ccl_stage_name(5) == ""
+    assert ccl.ccl_kernel_launches() >= 0
+    ms, n = ccl.ccl_stage_times()      # nothing recorded: no device work
+    assert n == 0 and ms == [0.0] * 5
+
+
 def test_set_option(lib):
+    assert ccl.ccl_set_option(ccl.CCL_OPT_STAGE_EVENTS, 0) == ccl.CCL_OK
     assert ccl.ccl_set_option(ccl.CCL_OPT_WALK_CAP, 5) == ccl.CCL_OK
     assert ccl.ccl_set_option(ccl.CCL_OPT_WALK_CAP, 0) == ccl.CCL_OK
     assert ccl.ccl_set_option(12345, 1) == ccl.CCL_ERR_INVALID_ARG
