@@ -31,7 +31,7 @@ CCL_OPT_STAGE_EVENTS = 2
 # every symbol include/ccl.h declares
 EXPORTED = ("ccl_label", "ccl_workspace_bytes", "ccl_label_ws", "ccl_label_host",
             "ccl_last_status", "ccl_status_string", "ccl_set_option", "ccl_stage_times",
-            "ccl_stage_name", "ccl_kernel_launches", "ccl_version")
+            "ccl_stage_name", "ccl_kernel_launches", "ccl_label_noalloc", "ccl_version")
 
 _lock = threading.Lock()
 _lib = None
@@ -73,6 +73,8 @@ def lib():
             L.ccl_stage_name.restype = ctypes.c_char_p
             L.ccl_kernel_launches.argtypes = []
             L.ccl_kernel_launches.restype = ctypes.c_longlong
+            L.ccl_label_noalloc.argtypes = [vp, i32, i32, i32, i32, i32, i32, vp, vp, vp]
+            L.ccl_label_noalloc.restype = i32
             L.ccl_version.argtypes = []
             L.ccl_version.restype = i32
             _lib = L
@@ -130,6 +132,18 @@ def ccl_stage_name(stage):
 
 def ccl_kernel_launches():
     return lib().ccl_kernel_launches()
+
+
+def ccl_label_noalloc(img, batch, H, W, pixel_bytes, connectivity, mode, labels, n_regions,
+                      stream):
+    """ccl_label without any device allocation (scratch in a fixed array of
+    CCL_NOALLOC_SCRATCH_BYTES inside the library); for callers that may not
+    allocate device memory.  Calls on one device must not overlap."""
+    return lib().ccl_label_noalloc(img, batch, H, W, pixel_bytes, connectivity, mode, labels,
+                                   n_regions, stream)
+
+
+CCL_NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
 def ccl_version():

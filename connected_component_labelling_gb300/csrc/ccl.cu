@@ -198,11 +198,12 @@ void k_seams_dispatch(int pb, int conn, int mode, const void* img, const uint16_
   CCL_DISPATCH(k_seams, L16, P, bm, cnt, g, cap, status);
 }
 
-int run(const void* img, int batch, int H, int W, int pb, int conn, int mode, int32_t* labels,
-        int32_t* n_out, const Layout& L, void* ws, cudaStream_t st) {
-  int* status = nullptr;
-  int rc = device_status_ptr(&status);
-  if (rc != CCL_OK) return rc;
+// The whole labelling pipeline on `st`: `ws` is the workspace (layout L),
+// `status` the device word the kernels flag limits in, `events` whether the
+// optional per-stage events may be recorded.
+int run_pipeline(const void* img, int batch, int H, int W, int pb, int conn, int mode,
+                 int32_t* labels, int32_t* n_out, const Layout& L, void* ws, int* status,
+                 bool events, cudaStream_t st) {
   char* base = (char*)ws;
   uint16_t* L16 = (uint16_t*)(base + L.offL16);
   uint32_t* bm = (uint32_t*)(base + L.offBm);
@@ -217,7 +218,7 @@ int run(const void* img, int batch, int H, int W, int pb, int conn, int mode, in
   const int capTile = (int)capT;
   const int capImg = (int)(capI > INT32_MAX ? INT32_MAX : capI);
   EventSet es;
-  const bool timed = take_event_set(&es);
+  const bool timed = events && take_event_set(&es);
   auto mark = [&](int k) {
     if (timed) cudaEventRecord(es.ev[k], st);
   };
@@ -247,6 +248,14 @@ int run(const void* img, int batch, int H, int W, int pb, int conn, int mode, in
   if (timed) keep_event_set(es);
   g_launches += n_out ? 8 : 7;
   return cudaPeekAtLastError() == cudaSuccess ? CCL_OK : CCL_ERR_CUDA;
+}
+
+int run(const void* img, int batch, int H, int W, int pb, int conn, int mode, int32_t* labels,
+        int32_t* n_out, const Layout& L, void* ws, cudaStream_t st) {
+  int* status = nullptr;
+  int rc = device_status_ptr(&status);
+  if (rc != CCL_OK) return rc;
+  return run_pipeline(img, batch, H, W, pb, conn, mode, labels, n_out, L, ws, status, true, st);
 }
 
 int empty_call(int batch, int32_t* n_out, cudaStream_t st) {
@@ -434,3 +443,85 @@ int ccl_last_status(ccl_stream_t stream) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Labelling without any device allocation.
+//
+// Some callers may not allocate device memory at all: a host application or
+// framework that owns the whole GPU memory budget (a fixed arena handed out
+// by its own allocator), or a latency-critical loop that cannot afford the
+// device-wide synchronisation cudaMalloc / cudaFree may imply.  For them
+// ccl_label_noalloc runs the same kernels as ccl_label with its scratch in a
+// fixed array that is part of this library's device image: every GPU that
+// loads the library holds CCL_NOALLOC_SCRATCH_BYTES for it until the process
+// exits.  Its first 256 bytes hold the call's device status word, the rest
+// the workspace that ccl_workspace_bytes() sizes.
+
+namespace {
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[CCL_NOALLOC_SCRATCH_BYTES];
+
+constexpr size_t NOALLOC_STATUS_BYTES = 256;
+
+// Device address of g_noalloc_scratch on the current device.  The array's
+// name in host code is only a host-side stand-in, so the address is asked
+// from the runtime once per device (with that device current) and cached.
+void* g_noalloc_addr[MAX_DEVICES] = {nullptr};
+
+int noalloc_scratch(char** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) return CCL_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mutex);
+  if (!g_noalloc_addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
+      cudaGetLastError();
+      return CCL_ERR_CUDA;
+    }
+    g_noalloc_addr[dev] = p;
+  }
+  *out = (char*)g_noalloc_addr[dev];
+  return CCL_OK;
+}
+
+// A device-side limit tripped during this call: every count becomes -1.
+__global__ void k_noalloc_report(const int* status, int32_t* n_out, int batch) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b < batch && *status != 0) n_out[b] = -1;
+}
+
+}  // namespace
+
+extern "C" int ccl_label_noalloc(const void* img, int batch, int H, int W, int pixel_bytes,
+                                 int connectivity, int mode, int32_t* labels_i32,
+                                 int32_t* n_regions_out, ccl_stream_t stream) {
+  bool empty = false;
+  int rc = validate(img, batch, H, W, pixel_bytes, connectivity, mode, labels_i32, n_regions_out,
+                    &empty);
+  if (rc != CCL_OK) return rc;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (empty) return empty_call(batch, n_regions_out, st);
+  Layout L;
+  rc = make_layout(batch, H, W, &L);
+  if (rc != CCL_OK) return rc;
+  if (L.total > (size_t)CCL_NOALLOC_SCRATCH_BYTES - NOALLOC_STATUS_BYTES) return CCL_ERR_TOO_LARGE;
+  char* scratch = nullptr;
+  rc = noalloc_scratch(&scratch);
+  if (rc != CCL_OK) return rc;
+  int* status = (int*)scratch;
+  // the array keeps the previous call's contents: the status word must start
+  // at zero; every workspace word the kernels read is written earlier in the
+  // same call
+  if (cudaMemsetAsync(status, 0, sizeof(int), st) != cudaSuccess) {
+    cudaGetLastError();
+    return CCL_ERR_CUDA;
+  }
+  rc = run_pipeline(img, batch, H, W, pixel_bytes, connectivity, mode, labels_i32, n_regions_out,
+                    L, scratch + NOALLOC_STATUS_BYTES, status, false, st);
+  if (rc == CCL_OK && n_regions_out) {
+    k_noalloc_report<<<(batch + 255) / 256, 256, 0, st>>>(status, n_regions_out, batch);
+    g_launches += 1;
+    if (cudaPeekAtLastError() != cudaSuccess) rc = CCL_ERR_CUDA;
+  }
+  return rc;
+}

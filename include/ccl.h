@@ -149,6 +149,39 @@ const char* ccl_stage_name(int stage);
 /* Number of CUDA kernels this library has launched in this process. */
 long long ccl_kernel_launches(void);
 
+/*
+ * ccl_label_noalloc -- ccl_label for callers that may not allocate device
+ * memory: a program whose device memory is owned and budgeted by someone
+ * else (a framework arena, a fixed-size pool), or a latency-critical loop
+ * that must not pay for the device-wide synchronisation cudaMalloc and
+ * cudaFree can cause.  It calls no cudaMalloc, cudaFree or allocating
+ * library routine.  The pages this library follows have no counterpart of
+ * this entry point; it exists only for such callers.
+ *
+ * Arguments, layout, results and ownership are those of ccl_label; the
+ * caller still provides img, labels_i32 and n_regions_out.  The scratch is a
+ * fixed array of CCL_NOALLOC_SCRATCH_BYTES inside the library's device image,
+ * held by every GPU that loads the library until the process exits; 256
+ * bytes of it are a status word and the rest must be at least
+ * ccl_workspace_bytes(...) for these arguments, else the call returns
+ * CCL_ERR_TOO_LARGE without doing anything (about 2.1 bytes per pixel:
+ * roughly 15 million pixels per call).
+ *  - The first call on a device looks up the array's device address (with
+ *    that device current) and caches it; make that first call before any
+ *    stream capture.
+ *  - Every call on a device shares the one array: calls whose work overlaps
+ *    on the GPU (other streams, or other threads) race and give wrong labels.
+ *    Serialise them, e.g. by using one stream.
+ *  - A device-side limit tripped during the call (see ccl_last_status) is
+ *    reported by writing -1 to every n_regions_out entry (pass
+ *    n_regions_out to be told); ccl_last_status does not see it.
+ */
+#define CCL_NOALLOC_SCRATCH_BYTES (32u << 20)
+int ccl_label_noalloc(const void* img, int batch, int H, int W,
+                      int pixel_bytes, int connectivity, int mode,
+                      int32_t* labels_i32, int32_t* n_regions_out,
+                      ccl_stream_t stream);
+
 /* Library version, as major*10000 + minor*100 + patch. */
 int ccl_version(void);
 

@@ -28,7 +28,7 @@ def test_header_declares_the_entry_points():
     names = declared_functions()
     for n in ("ccl_label", "ccl_label_ws", "ccl_workspace_bytes", "ccl_label_host",
               "ccl_last_status", "ccl_status_string", "ccl_set_option", "ccl_stage_times",
-              "ccl_stage_name", "ccl_kernel_launches", "ccl_version"):
+              "ccl_stage_name", "ccl_kernel_launches", "ccl_label_noalloc", "ccl_version"):
         assert n in names
     assert sorted(ccl.EXPORTED) == names
 
