@@ -50,6 +50,11 @@ def make_workload(name, device):
         img = wl.c4_sheet(device=device)
         return (dict(workload="c4_sheet_24000x33600_rgba", batch=1, H=wl.C4_H, W=wl.C4_W,
                      pixel_bytes=4, connectivity=8, mode="all"), img, 4, 8, 0)
+    if name.startswith("c4:"):      # the sheet generator at another size, e.g. c4:6000x8400
+        H, W = (int(v) for v in name[3:].split("x"))
+        img = wl.c4_sheet(device=device, H=H, W=W)
+        return (dict(workload="c4_sheet_%dx%d_rgba" % (H, W), batch=1, H=H, W=W,
+                     pixel_bytes=4, connectivity=8, mode="all"), img, 4, 8, 0)
     if name == "c0":
         img = wl.c0_drawing(device=device)
         return (dict(workload="c0_drawing_1024_rgba", batch=1, H=1024, W=1024, pixel_bytes=4,
@@ -397,7 +402,7 @@ def main():
 
     # ---- cpu baseline: the oracle on a band of the sheet, this host, 1 thread
     cpu_baseline = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline and args.workload == "c4":
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and args.workload.startswith("c4"):
         import oracle
         oracle.build()
         band = img[:CPU_BASELINE_ROWS].cpu().numpy().view(np.uint32)

@@ -28,7 +28,7 @@ std::atomic<long long> g_launches{0};
 
 // ---- optional per-stage CUDA events
 constexpr int NSTAGES = 5;
-const char* const STAGE_NAMES[NSTAGES] = {"tile_local", "seams", "compress", "scan", "number"};
+const char* const STAGE_NAMES[NSTAGES] = {"tile_local", "seams", "scan", "resolve", "number"};
 struct EventSet {
   int dev;
   cudaEvent_t ev[NSTAGES + 1];
@@ -235,13 +235,13 @@ int run_pipeline(const void* img, int batch, int H, int W, int pb, int conn, int
   mark(1);
   k_seams_dispatch(pb, conn, mode, img, L16, labels, bm, cnt, L, g, capImg, status, st);
   mark(2);
-  k_compress<<<grid, NT, 0, st>>>(L16, labels, g, capImg, status);
-  mark(3);
   k_scan_reduce<<<L.nScanBlocks, NT, 0, st>>>(cnt, L.nChunks, bsum);
   k_scan_top<<<1, NT, 0, st>>>(bsum, L.nScanBlocks);
   k_scan_down<<<L.nScanBlocks, NT, 0, st>>>(cnt, L.nChunks, bsum);
   if (n_out)
     k_region_counts<<<(batch + 255) / 256, 256, 0, st>>>(cnt, (long long)H * L.g.CPR, batch, n_out);
+  mark(3);
+  k_resolve<<<grid, NT, 0, st>>>(L16, labels, bm, cnt, g, capImg, status);
   mark(4);
   k_number<<<grid, NT, 0, st>>>(L16, labels, bm, cnt, g, status);
   mark(5);

@@ -1,7 +1,7 @@
 // ccl_kernels.cuh -- device code of the labelling library (sm_103a).
 //
 // The four stages of "every-colour" (blogs.fablnx.com) ch. 05 -- Start,
-// Connect, Collapse, Number -- as five kernels over 256 x TH pixel tiles:
+// Connect, Collapse, Number -- as kernels over 256 x TH pixel tiles:
 //
 //   k_tile_local  Start + Connect + Collapse inside one tile, in shared
 //                 memory.  A lane owns 8 consecutive pixels of a row; runs of
@@ -20,11 +20,12 @@
 //                 array with atomicMin and retry (ch. 06 Fig. 10;
 //                 bendabir.com, "Unions are parallel").  A leader that is
 //                 re-pointed leaves the bitmap and its chunk count.
-//   k_compress    Collapse for the border leaders: each points straight at
-//                 its final leader.
-//   k_scan_*      Number, first half: exclusive prefix sum of chunk counts
+//   k_scan_*      Number, first part: exclusive prefix sum of chunk counts
 //                 (ch. 08 switch 5; ch. 12, a prefix sum inside Number).
-//   k_number      Number, second half: a leader's label is 1 + the number of
+//   k_resolve     Collapse + Number for the border leaders re-pointed across
+//                 seams: each walks to its final leader and stores that
+//                 leader's label, negated, in its own slot.
+//   k_number      Number, last part: a leader's label is 1 + the number of
 //                 leaders before it in raster order; every pixel takes its
 //                 tile-local leader's label.
 //
@@ -290,14 +291,19 @@ __global__ void __launch_bounds__(NT) k_tile_local(const T* __restrict__ img, ui
   const int nval = max(0, min(PX, t.tw - xl));
   const unsigned vmask = (1u << nval) - 1u;
   const bool vec = g.vec_img && nval == PX;
+  // per row of this warp: foreground pixels, pixels equal to their left
+  // neighbour (same run), and the row position of the last run start left
+  // of this lane
   unsigned fgm[RPW], eqm[RPW];
+  int befm[RPW];
 
-  // ---- Start: each pixel points at the first pixel of its run in the row
+  // ---- Start: every pixel points at the first pixel of its run
 #pragma unroll
   for (int k = 0; k < RPW; ++k) {
     const int r = warp + k * NWARPS;
     fgm[k] = 0;
     eqm[k] = 0;
+    befm[k] = -1;
     if (r >= t.th) continue;   // warp-uniform
     uint32_t c[PX];
     load8<T>(im + (long long)(t.y0 + r) * g.W + t.x0 + xl, vec, nval, c);
@@ -309,10 +315,10 @@ __global__ void __launch_bounds__(NT) k_tile_local(const T* __restrict__ img, ui
     }
     const uint32_t cl = __shfl_up_sync(FULL, c[PX - 1], 1);
     const unsigned fgl = __shfl_up_sync(FULL, fg, 1);
-    unsigned eq = (lane > 0 && (fg & 1u) && ((fgl >> (PX - 1)) & 1u) && c[0] == cl) ? 1u : 0u;
+    unsigned eq = (lane > 0 && c[0] == cl) ? (fg & (fgl >> (PX - 1)) & 1u) : 0u;
 #pragma unroll
-    for (int j = 1; j < PX; ++j)
-      if (((fg >> j) & (fg >> (j - 1)) & 1u) && c[j] == c[j - 1]) eq |= 1u << j;
+    for (int j = 1; j < PX; ++j) eq |= (c[j] == c[j - 1] ? 1u : 0u) << j;
+    eq &= fg & (fg << 1 | 1u);
     const unsigned starts = fg & ~eq;
     int last = starts ? xl + 31 - __clz(starts) : -1;
 #pragma unroll
@@ -320,14 +326,14 @@ __global__ void __launch_bounds__(NT) k_tile_local(const T* __restrict__ img, ui
       const int y = __shfl_up_sync(FULL, last, o);
       if (lane >= o) last = max(last, y);
     }
-    int before = __shfl_up_sync(FULL, last, 1);
-    if (lane == 0) before = -1;
+    int cur = __shfl_up_sync(FULL, last, 1);
+    if (lane == 0) cur = -1;
+    befm[k] = cur;
     int pv[PX];
 #pragma unroll
     for (int j = 0; j < PX; ++j) {
-      const unsigned m = starts & ((2u << j) - 1u);
-      const int s = m ? xl + 31 - __clz(m) : before;
-      pv[j] = ((fg >> j) & 1u) ? r * TW + s : -1;
+      if ((starts >> j) & 1u) cur = xl + j;
+      pv[j] = ((fg >> j) & 1u) ? r * TW + cur : -1;
     }
     int4* pp = reinterpret_cast<int4*>(par + r * TW + xl);
     pp[0] = make_int4(pv[0], pv[1], pv[2], pv[3]);
@@ -338,9 +344,11 @@ __global__ void __launch_bounds__(NT) k_tile_local(const T* __restrict__ img, ui
   }
   __syncthreads();
 
-  // ---- Connect inside the tile: row above first; a pixel whose left
-  // neighbour has its colour leaves up-left and up to that neighbour.
-  // Neighbours outside the tile count as absent here (k_seams joins them).
+  // ---- Connect inside the tile.  Runs are already one node each, so every
+  // join goes to the row above; a pixel equal to its left neighbour leaves
+  // up-left and up to it (8-connectivity), or up when up-left matches too
+  // (4-connectivity).  Neighbours outside the tile count as absent here;
+  // k_seams makes those joins.
 #pragma unroll
   for (int k = 0; k < RPW; ++k) {
     const int r = warp + k * NWARPS;
@@ -351,31 +359,58 @@ __global__ void __launch_bounds__(NT) k_tile_local(const T* __restrict__ img, ui
     const uint32_t uL = __shfl_up_sync(FULL, u[PX - 1], 1);
     const uint32_t uR = __shfl_down_sync(FULL, u[0], 1);
     const unsigned fg = fgm[k], eq = eqm[k];
-    if (!fg) continue;
-    const bool hasL = lane > 0;
-    const bool hasR = lane < 31 && xl + PX < t.tw;
-    const int i0 = r * TW + xl;
+    unsigned mU = 0, mUL = 0, mUR = 0;
 #pragma unroll
     for (int j = 0; j < PX; ++j) {
-      if (!((fg >> j) & 1u)) continue;
       const uint32_t cj = c[j];
-      const bool eqL = (eq >> j) & 1u;
-      const bool eqU = cj == u[j];
-      const bool eqUL = j > 0 ? cj == u[j - 1] : (hasL && cj == uL);
-      if (CONN == 8) {
-        const bool eqUR = j < PX - 1 ? (((vmask >> (j + 1)) & 1u) && cj == u[j + 1]) : (hasR && cj == uR);
-        if (eqU && !eqL) union_s(par, i0 + j, i0 + j - TW, cap, status);
-        if (eqUL && !eqU && !eqL) union_s(par, i0 + j, i0 + j - TW - 1, cap, status);
-        if (eqUR && !eqU) union_s(par, i0 + j, i0 + j - TW + 1, cap, status);
-      } else {
-        if (eqU && !(eqL && eqUL)) union_s(par, i0 + j, i0 + j - TW, cap, status);
-      }
+      mU |= (cj == u[j] ? 1u : 0u) << j;
+      mUL |= (j > 0 ? cj == u[j - 1] : (lane > 0 && cj == uL)) ? (1u << j) : 0u;
+      if (CONN == 8)
+        mUR |= (j < PX - 1 ? cj == u[j + 1] : (lane < 31 && cj == uR)) ? (1u << j) : 0u;
+    }
+    mU &= fg;   // the pixel above is in the tile whenever this one is
+    mUL &= fg;
+    // up-right exists when the column to the right is in the tile
+    mUR &= fg & ((vmask >> 1) | ((lane < 31 && xl + PX < t.tw) ? 0x80u : 0u));
+    unsigned todo;
+    if (CONN == 8) {
+      const unsigned jU = mU & ~eq;
+      const unsigned jUL = mUL & ~mU & ~eq;
+      const unsigned jUR = mUR & ~mU;
+      todo = jU | (jUL << 8) | (jUR << 16);
+    } else {
+      todo = mU & ~(eq & mUL);
+    }
+    const int i0 = r * TW + xl;
+    while (todo) {
+      const int bpos = __ffs(todo) - 1;
+      todo &= todo - 1;
+      const int j = bpos & 7;
+      const int d = (bpos >> 3) == 0 ? 0 : ((bpos >> 3) == 1 ? -1 : 1);
+      union_s(par, i0 + j, i0 + j - TW + d, cap, status);
     }
   }
   __syncthreads();
 
-  // ---- Collapse inside the tile: one walk per run; write the leader map,
-  // the leader bitmap and the chunk counts; mark leaders on the border
+  // ---- Collapse inside the tile: one walk per run start, stored back at
+  // the start, then every pixel reads its run's leader
+#pragma unroll
+  for (int k = 0; k < RPW; ++k) {
+    const int r = warp + k * NWARPS;
+    if (r >= t.th) continue;   // warp-uniform
+    const unsigned starts = fgm[k] & ~eqm[k];
+    const int i0 = r * TW + xl;
+    const bool edgeRow = r == 0 || r == t.th - 1;
+    unsigned m = starts;
+    while (m) {
+      const int j = __ffs(m) - 1;
+      m &= m - 1;
+      const int root = find_s(par, i0 + j, cap, status);
+      par[i0 + j] = root;
+      if (edgeRow || xl + j == 0) mark[root] = 1;
+    }
+  }
+  __syncwarp();
   unsigned rootm[RPW];
 #pragma unroll
   for (int k = 0; k < RPW; ++k) {
@@ -384,20 +419,19 @@ __global__ void __launch_bounds__(NT) k_tile_local(const T* __restrict__ img, ui
     if (r >= t.th) continue;   // warp-uniform
     const unsigned fg = fgm[k], starts = fg & ~eqm[k];
     const int i0 = r * TW + xl;
-    const bool edgeRow = r == 0 || r == t.th - 1;
+    // a run entering from the left lane: its start (same row, same warp)
+    // already holds the leader
+    int cur = ((fg & ~starts) & 1u) ? par[r * TW + befm[k]] : 0;
     uint32_t lv[PX];
     unsigned rm = 0;
-    int cur = 0;
 #pragma unroll
     for (int j = 0; j < PX; ++j) {
-      lv[j] = LBG;
-      if (!((fg >> j) & 1u)) continue;
-      if (j == 0 || ((starts >> j) & 1u)) cur = find_s(par, i0 + j, cap, status);
-      lv[j] = (uint32_t)cur;
-      if (cur == i0 + j) rm |= 1u << j;
-      const int x = xl + j;
-      if (edgeRow || x == 0 || x == t.tw - 1) mark[cur] = 1;
+      if ((starts >> j) & 1u) cur = par[i0 + j];
+      lv[j] = ((fg >> j) & 1u) ? (uint32_t)cur : (uint32_t)LBG;
+      rm |= (cur == i0 + j && ((starts >> j) & 1u)) ? (1u << j) : 0u;
     }
+    const int jr = t.tw - 1 - xl;   // the tile's right column, if this lane has it
+    if (jr >= 0 && jr < PX && ((fg >> jr) & 1u)) mark[lv[jr]] = 1;
     uint16_t* lrow = Li + (long long)(t.y0 + r) * g.W + t.x0 + xl;
     if (g.vec_out && nval == PX) {
       *reinterpret_cast<uint4*>(lrow) = make_uint4(lv[0] | (lv[1] << 16), lv[2] | (lv[3] << 16),
@@ -422,10 +456,11 @@ __global__ void __launch_bounds__(NT) k_tile_local(const T* __restrict__ img, ui
 #pragma unroll
   for (int k = 0; k < RPW; ++k) {
     const int r = warp + k * NWARPS;
-    if (r >= t.th || !rootm[k]) continue;
-#pragma unroll
-    for (int j = 0; j < PX; ++j) {
-      if (((rootm[k] >> j) & 1u) && mark[r * TW + xl + j]) {
+    unsigned m = rootm[k];
+    while (m) {
+      const int j = __ffs(m) - 1;
+      m &= m - 1;
+      if (mark[r * TW + xl + j]) {
         const int gi = (t.y0 + r) * g.W + t.x0 + xl + j;
         Pi[gi] = gi;
       }
@@ -482,29 +517,6 @@ __global__ void __launch_bounds__(NT) k_seams(const T* __restrict__ img, const u
     else if (k < nTop + nSide) { y = t.y0 + 1 + (k - nTop); x = t.x0; }
     else { y = t.y0 + 1 + (k - nTop - nSide); x = t.x0 + t.tw - 1; }
     seam_joins<T, CONN, BIN>(im, Li, Pi, bmi, cnti, g, y, x, t.y0, t.x0, cap, status);
-  }
-}
-
-// Collapse for the leaders that took part in seam joins: every such
-// leader's tile region touches the tile border, so walking from the border
-// pixels reaches all of them.
-__global__ void __launch_bounds__(NT) k_compress(const uint16_t* __restrict__ L16, int32_t* P, Geom g,
-                                                 int cap, int* status) {
-  const TileCoord t = tile_coord(g);
-  const long long ioff = (long long)t.b * g.HW;
-  const uint16_t* Li = L16 + ioff;
-  int32_t* Pi = P + ioff;
-  const int n = 2 * t.tw + 2 * t.th;
-  for (int k = threadIdx.x; k < n; k += NT) {
-    int y, x;
-    if (k < t.tw) { y = t.y0; x = t.x0 + k; }
-    else if (k < 2 * t.tw) { y = t.y0 + t.th - 1; x = t.x0 + (k - t.tw); }
-    else if (k < 2 * t.tw + t.th) { y = t.y0 + (k - 2 * t.tw); x = t.x0; }
-    else { y = t.y0 + (k - 2 * t.tw - t.th); x = t.x0 + t.tw - 1; }
-    const int r = leader_of(Li, y, x, g);
-    if (r < 0) continue;
-    const int root = find_g(Pi, r, (int)g.HW, cap, status);
-    if (root >= 0 && root != r) atomicMin(Pi + r, root);
   }
 }
 
@@ -608,10 +620,59 @@ __device__ __forceinline__ int number_of(int gidx, const uint32_t* bmi, const ui
   return (int)(offi[(long long)gy * g.CPR + (gx >> LOG_TW)] - base0 + s + 1u);
 }
 
-// Number: labels of the tile's leaders from the bitmap and the chunk offsets,
-// then every pixel takes its tile-local leader's label.  The labels buffer
-// holds the global parent slots of border leaders until this kernel
-// overwrites them; a tile reads only its own slots, before writing.
+// Collapse + Number for the leaders re-pointed across seams.  Every such
+// leader's tile region touches the tile border, so starting from the border
+// pixels reaches all of them.  Each walks to its final leader (halving on
+// the way), takes that leader's label, and stores it negated in its own
+// slot.  A walk that meets a slot already holding a negated label stops
+// there: every node on a walk belongs to the same region.
+__global__ void __launch_bounds__(NT) k_resolve(const uint16_t* __restrict__ L16, int32_t* P,
+                                                const uint32_t* __restrict__ bm,
+                                                const uint32_t* __restrict__ off, Geom g, int cap,
+                                                int* status) {
+  const TileCoord t = tile_coord(g);
+  const long long ioff = (long long)t.b * g.HW;
+  const uint16_t* Li = L16 + ioff;
+  int32_t* Pi = P + ioff;
+  const uint32_t* bmi = bm + (long long)t.b * g.H * g.WPR;
+  const uint32_t* offi = off + (long long)t.b * g.H * g.CPR;
+  const uint32_t base0 = offi[0];
+  const int n = (int)g.HW;
+  const int np = 2 * t.tw + 2 * t.th;
+  for (int k = threadIdx.x; k < np; k += NT) {
+    int y, x;
+    if (k < t.tw) { y = t.y0; x = t.x0 + k; }
+    else if (k < 2 * t.tw) { y = t.y0 + t.th - 1; x = t.x0 + (k - t.tw); }
+    else if (k < 2 * t.tw + t.th) { y = t.y0 + (k - 2 * t.tw); x = t.x0; }
+    else { y = t.y0 + (k - 2 * t.tw - t.th); x = t.x0 + t.tw - 1; }
+    const int r = leader_of(Li, y, x, g);
+    if (r < 0) continue;
+    const int v = __ldcg(Pi + r);
+    if (v == r || v < 0) continue;   // still a leader, or already resolved
+    int node = r, lab = 0, s = 0;
+    for (; s < cap; ++s) {
+      const int p = __ldcg(Pi + node);
+      if (p < 0) { lab = -p; break; }
+      if (p == node) { lab = number_of(node, bmi, offi, base0, g, status); break; }
+      if (p >= n) { raise_flag(status, FLAG_INTERNAL); break; }
+      const int gp = __ldcg(Pi + p);
+      if (gp < 0) { lab = -gp; break; }
+      if (gp == p) { lab = number_of(p, bmi, offi, base0, g, status); break; }
+      if (gp >= n) { raise_flag(status, FLAG_INTERNAL); break; }
+      atomicMin(Pi + node, gp);   // a slot holding a negated label keeps it
+      node = gp;
+    }
+    if (s == cap) raise_flag(status, FLAG_WALK_CAP);
+    if (lab > 0) atomicMin(Pi + r, -lab);
+  }
+}
+
+// Number: labels of the tile's leaders (from the bitmap and the chunk
+// offsets, or, for leaders re-pointed across a seam, the negated label
+// k_resolve left in their slot), then every pixel takes its tile-local
+// leader's label.  The labels buffer holds the slots of border leaders
+// until this kernel overwrites it; a tile reads only its own slots, before
+// writing.
 __global__ void __launch_bounds__(NT) k_number(const uint16_t* __restrict__ L16, int32_t* labels,
                                                const uint32_t* __restrict__ bm,
                                                const uint32_t* __restrict__ off, Geom g, int* status) {
@@ -646,7 +707,6 @@ __global__ void __launch_bounds__(NT) k_number(const uint16_t* __restrict__ L16,
                                 : ((lw[k][j >> 1] & 0xFFFF0000u) | l);
       }
     }
-    // leaders of this row: rank within the row from the bitmap
     // word w of the row segment belongs to lanes 4w..4w+3; lane 4w counts it
     const uint32_t w = xl < t.tw ? bmi[(long long)(t.y0 + r) * g.WPR + ((t.x0 + xl) >> 5)] : 0u;
     const uint32_t mine = ((lane & 3) == 0) ? __popc(w) : 0u;
@@ -656,45 +716,25 @@ __global__ void __launch_bounds__(NT) k_number(const uint16_t* __restrict__ L16,
       const uint32_t y = __shfl_up_sync(FULL, inc, o);
       if (lane >= o) inc += y;
     }
-    // leaders in the words before this lane's word
     const uint32_t pre = __shfl_sync(FULL, inc - mine, lane & ~3);
     const uint32_t o = offi[(long long)(t.y0 + r) * g.CPR + t.tx] - base0;
     const int i0 = r * TW + xl;
+    unsigned lead = 0;   // pixels of this lane that are their own tile-local leader
 #pragma unroll
-    for (int j = 0; j < PX; ++j) {
-      const int l = (int)((lw[k][j >> 1] >> (16 * (j & 1))) & 0xFFFFu);
-      if (l != i0 + j) continue;   // not a leader
-      const int bit = (xl + j) & 31;
-      if ((w >> bit) & 1u) {
+    for (int j = 0; j < PX; ++j)
+      lead |= (((lw[k][j >> 1] >> (16 * (j & 1))) & 0xFFFFu) == (uint32_t)(i0 + j)) ? (1u << j) : 0u;
+    const unsigned wbits = (w >> ((xl & 31))) & 0xFFu;
+    unsigned m = lead;
+    while (m) {
+      const int j = __ffs(m) - 1;
+      m &= m - 1;
+      if ((wbits >> j) & 1u) {
+        const int bit = (xl + j) & 31;
         lab[i0 + j] = (int)(o + pre + __popc(w & ((1u << bit) - 1u)) + 1u);
       } else {
-        // re-pointed across a seam: k_compress left the final leader here
-        const int gi = (t.y0 + r) * g.W + t.x0 + xl + j;
-        const int gg = Pi[gi];
-        const int gy = div_w(gg, g), gx = gg - gy * g.W;
-        if (gg >= 0 && gy >= t.y0 && gy < t.y0 + t.th && gx >= t.x0 && gx < t.x0 + t.tw)
-          lab[i0 + j] = -1 - (((gy - t.y0) << LOG_TW) + (gx - t.x0));
-        else
-          lab[i0 + j] = number_of(gg, bmi, offi, base0, g, status);
-      }
-    }
-  }
-  __syncthreads();
-  // leaders whose final leader is in this tile take its label
-#pragma unroll
-  for (int k = 0; k < RPW; ++k) {
-    const int r = warp + k * NWARPS;
-    if (r >= t.th) continue;
-    const int i0 = r * TW + xl;
-#pragma unroll
-    for (int j = 0; j < PX; ++j) {
-      const int l = (int)((lw[k][j >> 1] >> (16 * (j & 1))) & 0xFFFFu);
-      if (l != i0 + j) continue;
-      const int v = lab[i0 + j];
-      if (v < 0) {
-        const int w = lab[-1 - v];
-        if (w <= 0) raise_flag(status, FLAG_INTERNAL);
-        lab[i0 + j] = w > 0 ? w : 0;
+        const int v = Pi[(long long)(t.y0 + r) * g.W + t.x0 + xl + j];
+        if (v >= 0) raise_flag(status, FLAG_INTERNAL);
+        lab[i0 + j] = v < 0 ? -v : 0;
       }
     }
   }
@@ -706,8 +746,8 @@ __global__ void __launch_bounds__(NT) k_number(const uint16_t* __restrict__ L16,
     int out[PX];
 #pragma unroll
     for (int j = 0; j < PX; ++j) {
-      const int l = (int)((lw[k][j >> 1] >> (16 * (j & 1))) & 0xFFFFu);
-      out[j] = (l == LBG || l >= TILE) ? 0 : lab[l];
+      const uint32_t l = (lw[k][j >> 1] >> (16 * (j & 1))) & 0xFFFFu;
+      out[j] = l < (uint32_t)TILE ? lab[l] : 0;
     }
     int32_t* orow = Pi + (long long)(t.y0 + r) * g.W + t.x0 + xl;
     if (vec) {

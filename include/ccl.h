@@ -137,7 +137,7 @@ int ccl_set_option(int option, long long value);
  * Per-stage device timing.  While option CCL_OPT_STAGE_EVENTS is non-zero
  * every labelling call records a CUDA event on its own stream before its
  * first kernel and after each stage (the stages are named by
- * ccl_stage_name: 0 tile_local, 1 seams, 2 compress, 3 scan, 4 number).
+ * ccl_stage_name: 0 tile_local, 1 seams, 2 scan, 3 resolve, 4 number).
  * ccl_stage_times waits for those events, writes the summed milliseconds of
  * each stage over all recorded calls into ms_sum[0..max_stages) and the call
  * count into *n_calls (either pointer may be NULL), forgets the recorded

@@ -100,7 +100,7 @@ def test_workspace_checks_on_host(lib):
 
 def test_stage_names_and_counter(lib):
     assert [ccl.ccl_stage_name(k) for k in range(5)] == [
-        "tile_local", "seams", "compress", "scan", "number"]
+        "tile_local", "seams", "scan", "resolve", "number"]
     assert ccl.ccl_stage_name(5) == ""
     assert ccl.ccl_kernel_launches() >= 0
     ms, n = ccl.ccl_stage_times()      # nothing recorded: no device work
