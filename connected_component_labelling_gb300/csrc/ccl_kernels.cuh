@@ -11,7 +11,8 @@
 //                 skip what the left neighbour already joins (ch. 08 "First,
 //                 the order of the joins" and switch 2, the Wu-Otoo-Suzuki
 //                 scan mask); walks halve paths with the same atomic minimum
-//                 (switch 3).  Output: a 2-byte tile-local leader per pixel,
+//                 (switch 3).  Output: a 2-byte leader map (a pixel's run
+//                 start; for a run start, its tile-local leader),
 //                 a leader bitmap, a leader count per 256-pixel chunk of a
 //                 row, and a global parent slot (its own raster index) for
 //                 every leader whose region touches the tile border.
@@ -254,11 +255,21 @@ __device__ __forceinline__ void union_g(int* P, int a, int b, uint32_t* bm, uint
 }
 
 // image raster index of the tile-local leader of pixel (y, x), -1 for background
+// The leader map holds, for every pixel, its run start, and for every run
+// start its tile-local leader: two hops give the leader.
 __device__ __forceinline__ int leader_of(const uint16_t* Li, int y, int x, const Geom& g) {
-  const uint16_t l = Li[(long long)y * g.W + x];
+  const int ty0 = y & ~(TH - 1), tx0 = x & ~(TW - 1);
+  uint16_t l = Li[(long long)y * g.W + x];
   if (l >= TILE) return -1;   // background (LBG)
-  const int ly = (y & ~(TH - 1)) + (l >> LOG_TW), lx = (x & ~(TW - 1)) + (l & (TW - 1));
+  int ly = ty0 + (l >> LOG_TW), lx = tx0 + (l & (TW - 1));
   if (ly >= g.H || lx >= g.W) return -1;   // only a corrupted map can get here
+  if (ly != y || lx != x) {
+    l = Li[(long long)ly * g.W + lx];
+    if (l >= TILE) return -1;
+    ly = ty0 + (l >> LOG_TW);
+    lx = tx0 + (l & (TW - 1));
+    if (ly >= g.H || lx >= g.W) return -1;
+  }
   return ly * g.W + lx;
 }
 
@@ -339,6 +350,21 @@ __global__ void __launch_bounds__(NT) k_tile_local(const T* __restrict__ img, ui
     pp[0] = make_int4(pv[0], pv[1], pv[2], pv[3]);
     pp[1] = make_int4(pv[4], pv[5], pv[6], pv[7]);
     st8s<T>(col + r * TW + xl, c);
+    // leader map, first pass: every pixel's run start (background LBG);
+    // Collapse overwrites the entries of run starts with their leader
+    uint32_t lw[PX / 2];
+#pragma unroll
+    for (int q = 0; q < PX / 2; ++q)
+      lw[q] = (pv[2 * q] < 0 ? LBG : (uint32_t)pv[2 * q]) |
+              ((pv[2 * q + 1] < 0 ? LBG : (uint32_t)pv[2 * q + 1]) << 16);
+    uint16_t* lrow = Li + (long long)(t.y0 + r) * g.W + t.x0 + xl;
+    if (g.vec_out && nval == PX) {
+      *reinterpret_cast<uint4*>(lrow) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+    } else {
+#pragma unroll
+      for (int j = 0; j < PX; ++j)
+        if (j < nval) lrow[j] = (uint16_t)(lw[j >> 1] >> (16 * (j & 1)));
+    }
     fgm[k] = fg;
     eqm[k] = eq;
   }
@@ -387,60 +413,52 @@ __global__ void __launch_bounds__(NT) k_tile_local(const T* __restrict__ img, ui
       todo &= todo - 1;
       const int j = bpos & 7;
       const int d = (bpos >> 3) == 0 ? 0 : ((bpos >> 3) == 1 ? -1 : 1);
-      union_s(par, i0 + j, i0 + j - TW + d, cap, status);
+      const int a = i0 + j, b = i0 + j - TW + d;
+      if (par[a] != par[b]) union_s(par, a, b, cap, status);   // else joined already
     }
   }
   __syncthreads();
 
-  // ---- Collapse inside the tile: one walk per run start, stored back at
-  // the start, then every pixel reads its run's leader
-#pragma unroll
-  for (int k = 0; k < RPW; ++k) {
-    const int r = warp + k * NWARPS;
-    if (r >= t.th) continue;   // warp-uniform
-    const unsigned starts = fgm[k] & ~eqm[k];
-    const int i0 = r * TW + xl;
-    const bool edgeRow = r == 0 || r == t.th - 1;
-    unsigned m = starts;
-    while (m) {
-      const int j = __ffs(m) - 1;
-      m &= m - 1;
-      const int root = find_s(par, i0 + j, cap, status);
-      par[i0 + j] = root;
-      if (edgeRow || xl + j == 0) mark[root] = 1;
-    }
-  }
-  __syncwarp();
+  // ---- Collapse inside the tile: one walk per run start.  The leader is
+  // stored back at the start (so par and the leader map give every pixel's
+  // leader in two hops: pixel -> run start -> leader); the leader bitmap,
+  // chunk counts and border marks follow from the starts alone
   unsigned rootm[RPW];
 #pragma unroll
   for (int k = 0; k < RPW; ++k) {
     const int r = warp + k * NWARPS;
     rootm[k] = 0;
     if (r >= t.th) continue;   // warp-uniform
-    const unsigned fg = fgm[k], starts = fg & ~eqm[k];
+    const unsigned starts = fgm[k] & ~eqm[k];
     const int i0 = r * TW + xl;
-    // a run entering from the left lane: its start (same row, same warp)
-    // already holds the leader
-    int cur = ((fg & ~starts) & 1u) ? par[r * TW + befm[k]] : 0;
-    uint32_t lv[PX];
-    unsigned rm = 0;
-#pragma unroll
-    for (int j = 0; j < PX; ++j) {
-      if ((starts >> j) & 1u) cur = par[i0 + j];
-      lv[j] = ((fg >> j) & 1u) ? (uint32_t)cur : (uint32_t)LBG;
-      rm |= (cur == i0 + j && ((starts >> j) & 1u)) ? (1u << j) : 0u;
-    }
-    const int jr = t.tw - 1 - xl;   // the tile's right column, if this lane has it
-    if (jr >= 0 && jr < PX && ((fg >> jr) & 1u)) mark[lv[jr]] = 1;
+    const bool edgeRow = r == 0 || r == t.th - 1;
     uint16_t* lrow = Li + (long long)(t.y0 + r) * g.W + t.x0 + xl;
-    if (g.vec_out && nval == PX) {
-      *reinterpret_cast<uint4*>(lrow) = make_uint4(lv[0] | (lv[1] << 16), lv[2] | (lv[3] << 16),
-                                                   lv[4] | (lv[5] << 16), lv[6] | (lv[7] << 16));
-    } else {
-#pragma unroll
-      for (int j = 0; j < PX; ++j)
-        if (j < nval) lrow[j] = (uint16_t)lv[j];
+    unsigned m = starts, rm = 0;
+    while (m) {
+      const int j = __ffs(m) - 1;
+      m &= m - 1;
+      const int root = find_s(par, i0 + j, cap, status);
+      par[i0 + j] = root;
+      if (root == i0 + j) rm |= 1u << j;
+      else lrow[j] = (uint16_t)root;
+      if (edgeRow || xl + j == 0) mark[root] = 1;
     }
+    rootm[k] = rm;
+  }
+  __syncwarp();
+#pragma unroll
+  for (int k = 0; k < RPW; ++k) {
+    const int r = warp + k * NWARPS;
+    if (r >= t.th) continue;   // warp-uniform
+    // the tile's right column: mark the leader of its run
+    const int jr = t.tw - 1 - xl;
+    const unsigned fg = fgm[k], starts = fg & ~eqm[k];
+    if (jr >= 0 && jr < PX && ((fg >> jr) & 1u)) {
+      const unsigned sm = starts & ((2u << jr) - 1u);
+      const int s = sm ? xl + 31 - __clz(sm) : befm[k];
+      mark[par[r * TW + s]] = 1;
+    }
+    const unsigned rm = rootm[k];
     const unsigned b1 = __shfl_down_sync(FULL, rm, 1);
     const unsigned b2 = __shfl_down_sync(FULL, rm, 2);
     const unsigned b3 = __shfl_down_sync(FULL, rm, 3);
@@ -448,7 +466,6 @@ __global__ void __launch_bounds__(NT) k_tile_local(const T* __restrict__ img, ui
       bmi[(long long)(t.y0 + r) * g.WPR + ((t.x0 + xl) >> 5)] = rm | (b1 << 8) | (b2 << 16) | (b3 << 24);
     const int n = warp_sum(__popc(rm));
     if (lane == 0) cnti[(long long)(t.y0 + r) * g.CPR + t.tx] = (uint32_t)n;
-    rootm[k] = rm;
   }
   __syncthreads();
 
@@ -669,14 +686,15 @@ __global__ void __launch_bounds__(NT) k_resolve(const uint16_t* __restrict__ L16
 
 // Number: labels of the tile's leaders (from the bitmap and the chunk
 // offsets, or, for leaders re-pointed across a seam, the negated label
-// k_resolve left in their slot), then every pixel takes its tile-local
-// leader's label.  The labels buffer holds the slots of border leaders
+// k_resolve left in their slot), then every pixel takes the label of its
+// tile-local leader, two hops away in the leader map.  The labels buffer holds the slots of border leaders
 // until this kernel overwrites it; a tile reads only its own slots, before
 // writing.
 __global__ void __launch_bounds__(NT) k_number(const uint16_t* __restrict__ L16, int32_t* labels,
                                                const uint32_t* __restrict__ bm,
                                                const uint32_t* __restrict__ off, Geom g, int* status) {
   __shared__ __align__(16) int lab[TILE];
+  __shared__ __align__(16) uint16_t lmap[TILE];   // the tile's leader map
   const TileCoord t = tile_coord(g);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, xl = lane * PX;
   const long long ioff = (long long)t.b * g.HW;
@@ -707,6 +725,7 @@ __global__ void __launch_bounds__(NT) k_number(const uint16_t* __restrict__ L16,
                                 : ((lw[k][j >> 1] & 0xFFFF0000u) | l);
       }
     }
+    *reinterpret_cast<uint4*>(lmap + r * TW + xl) = make_uint4(lw[k][0], lw[k][1], lw[k][2], lw[k][3]);
     // word w of the row segment belongs to lanes 4w..4w+3; lane 4w counts it
     const uint32_t w = xl < t.tw ? bmi[(long long)(t.y0 + r) * g.WPR + ((t.x0 + xl) >> 5)] : 0u;
     const uint32_t mine = ((lane & 3) == 0) ? __popc(w) : 0u;
@@ -746,8 +765,10 @@ __global__ void __launch_bounds__(NT) k_number(const uint16_t* __restrict__ L16,
     int out[PX];
 #pragma unroll
     for (int j = 0; j < PX; ++j) {
+      // pixel -> run start -> leader
       const uint32_t l = (lw[k][j >> 1] >> (16 * (j & 1))) & 0xFFFFu;
-      out[j] = l < (uint32_t)TILE ? lab[l] : 0;
+      const uint32_t ld = l < (uint32_t)TILE ? (uint32_t)lmap[l] : 0xFFFFu;
+      out[j] = ld < (uint32_t)TILE ? lab[ld] : 0;
     }
     int32_t* orow = Pi + (long long)(t.y0 + r) * g.W + t.x0 + xl;
     if (vec) {
