@@ -67,7 +67,7 @@ struct Layout {
   long long nTiles;
   long long nChunks;     // batch * H * CPR
   int nScanBlocks;
-  size_t offL16, offBm, offCnt, offBsum, total;
+  size_t offL16, offBm, offCnt, offBsum, offRec, offList, offBcnt, total;
 };
 
 int make_layout(int batch, int H, int W, Layout* L) {
@@ -102,6 +102,12 @@ int make_layout(int batch, int H, int W, Layout* L) {
   o = align_up(o + (size_t)(L->nChunks + 1) * sizeof(uint32_t), 256);
   L->offBsum = o;
   o = align_up(o + (size_t)(L->nScanBlocks + 1) * sizeof(uint32_t), 256);
+  L->offRec = o;
+  o = align_up(o + (size_t)L->nTiles * 4 * TH * sizeof(uint32_t), 256);
+  L->offList = o;
+  o = align_up(o + (size_t)L->nTiles * BLCAP * sizeof(uint16_t), 256);
+  L->offBcnt = o;
+  o = align_up(o + (size_t)L->nTiles * sizeof(uint32_t), 256);
   L->total = o;
   return CCL_OK;
 }
@@ -187,15 +193,15 @@ int device_pool(cudaMemPool_t* out) {
   } while (0)
 
 void k_tile_local_dispatch(int pb, int conn, int mode, const void* img, uint16_t* L16, int32_t* P,
-                           uint32_t* bm, uint32_t* cnt, const Layout& L, const Geom& g, int cap,
-                           int* status, cudaStream_t st) {
-  CCL_DISPATCH(k_tile_local, L16, P, bm, cnt, g, cap, status);
+                           uint32_t* bm, uint32_t* cnt, const Border& bd, const Layout& L,
+                           const Geom& g, int cap, int* status, cudaStream_t st) {
+  CCL_DISPATCH(k_tile_local, L16, P, bm, cnt, bd, g, cap, status);
 }
 
 void k_seams_dispatch(int pb, int conn, int mode, const void* img, const uint16_t* L16, int32_t* P,
-                      uint32_t* bm, uint32_t* cnt, const Layout& L, const Geom& g, int cap,
-                      int* status, cudaStream_t st) {
-  CCL_DISPATCH(k_seams, L16, P, bm, cnt, g, cap, status);
+                      uint32_t* bm, uint32_t* cnt, const Border& bd, const Layout& L,
+                      const Geom& g, int cap, int* status, cudaStream_t st) {
+  CCL_DISPATCH(k_seams, L16, P, bm, cnt, bd, g, cap, status);
 }
 
 // The whole labelling pipeline on `st`: `ws` is the workspace (layout L),
@@ -209,6 +215,10 @@ int run_pipeline(const void* img, int batch, int H, int W, int pb, int conn, int
   uint32_t* bm = (uint32_t*)(base + L.offBm);
   uint32_t* cnt = (uint32_t*)(base + L.offCnt);
   uint32_t* bsum = (uint32_t*)(base + L.offBsum);
+  Border bd;
+  bd.rec = (uint32_t*)(base + L.offRec);
+  bd.list = (uint16_t*)(base + L.offList);
+  bd.cnt = (uint32_t*)(base + L.offBcnt);
   long long capT = TILE + 1, capI = L.g.HW + 1;
   const long long user = g_walk_cap;
   if (user > 0) {
@@ -231,9 +241,9 @@ int run_pipeline(const void* img, int batch, int H, int W, int pb, int conn, int
   g.vec_out = (W % 8 == 0) && ((uintptr_t)labels % 16 == 0);
   const unsigned grid = (unsigned)L.nTiles;
   mark(0);
-  k_tile_local_dispatch(pb, conn, mode, img, L16, labels, bm, cnt, L, g, capTile, status, st);
+  k_tile_local_dispatch(pb, conn, mode, img, L16, labels, bm, cnt, bd, L, g, capTile, status, st);
   mark(1);
-  k_seams_dispatch(pb, conn, mode, img, L16, labels, bm, cnt, L, g, capImg, status, st);
+  k_seams_dispatch(pb, conn, mode, img, L16, labels, bm, cnt, bd, L, g, capImg, status, st);
   mark(2);
   k_scan_reduce<<<L.nScanBlocks, NT, 0, st>>>(cnt, L.nChunks, bsum);
   k_scan_top<<<1, NT, 0, st>>>(bsum, L.nScanBlocks);
@@ -241,7 +251,8 @@ int run_pipeline(const void* img, int batch, int H, int W, int pb, int conn, int
   if (n_out)
     k_region_counts<<<(batch + 255) / 256, 256, 0, st>>>(cnt, (long long)H * L.g.CPR, batch, n_out);
   mark(3);
-  k_resolve<<<grid, NT, 0, st>>>(L16, labels, bm, cnt, g, capImg, status);
+  k_resolve<<<(unsigned)((L.nTiles + NWARPS - 1) / NWARPS), NT, 0, st>>>(bd, L.nTiles, labels, bm, cnt,
+                                                                          g, capImg, status);
   mark(4);
   k_number<<<grid, NT, 0, st>>>(L16, labels, bm, cnt, g, status);
   mark(5);

@@ -24,8 +24,9 @@
 //   k_scan_*      Number, first part: exclusive prefix sum of chunk counts
 //                 (ch. 08 switch 5; ch. 12, a prefix sum inside Number).
 //   k_resolve     Collapse + Number for the border leaders re-pointed across
-//                 seams: each walks to its final leader and stores that
-//                 leader's label, negated, in its own slot.
+//                 seams (from the tiles' border lists): each walks to its
+//                 final leader and stores that leader's label, negated, in
+//                 its own slot.
 //   k_number      Number, last part: a leader's label is 1 + the number of
 //                 leaders before it in raster order; every pixel takes its
 //                 tile-local leader's label.
@@ -72,13 +73,25 @@ struct Geom {
   int vec_out;                  // leader-map and label rows allow vector access
 };
 
+// Per-tile border data written by k_tile_local:
+//  rec   4*TH words per tile: colours of the left column, leaders of the left
+//        column, colours of the right column, leaders of the right column
+//        (leaders as image raster indices, -1 for background);
+//  list  up to BLCAP tile-local indices per tile: leaders whose region
+//        touches the tile border (count in cnt).
+constexpr int BLCAP = 2 * TW + 2 * TH;
+struct Border {
+  uint32_t* rec;
+  uint16_t* list;
+  uint32_t* cnt;
+};
+
 struct TileCoord {
   int b, tx, y0, x0, th, tw;
 };
 
-__device__ __forceinline__ TileCoord tile_coord(const Geom& g) {
+__device__ __forceinline__ TileCoord tile_coord_of(const Geom& g, long long tile) {
   TileCoord t;
-  const long long tile = blockIdx.x;
   t.b = (int)(tile / g.tilesPerImage);
   const int rest = (int)(tile - (long long)t.b * g.tilesPerImage);
   const int ty = rest / g.tilesX;
@@ -89,6 +102,8 @@ __device__ __forceinline__ TileCoord tile_coord(const Geom& g) {
   t.tw = min(TW, g.W - t.x0);
   return t;
 }
+
+__device__ __forceinline__ TileCoord tile_coord(const Geom& g) { return tile_coord_of(g, blockIdx.x); }
 
 __device__ __forceinline__ int div_w(int d, const Geom& g) {
   return (int)(((unsigned long long)(unsigned)d * g.wmagic) >> g.wshift);
@@ -284,9 +299,10 @@ __device__ __forceinline__ int warp_sum(int v) {
 template <typename T, int CONN, bool BIN>
 __global__ void __launch_bounds__(NT) k_tile_local(const T* __restrict__ img, uint16_t* __restrict__ L16,
                                                    int32_t* __restrict__ P, uint32_t* __restrict__ bm,
-                                                   uint32_t* __restrict__ cnt, Geom g, int cap,
-                                                   int* status) {
+                                                   uint32_t* __restrict__ cnt, Border bd, Geom g,
+                                                   int cap, int* status) {
   __shared__ __align__(16) T col[TILE];
+  __shared__ int nborder;
   __shared__ __align__(16) int par[TILE];
   __shared__ __align__(16) uint8_t mark[TILE];
   const TileCoord t = tile_coord(g);
@@ -299,6 +315,7 @@ __global__ void __launch_bounds__(NT) k_tile_local(const T* __restrict__ img, ui
   uint32_t* cnti = cnt + (long long)t.b * g.H * g.CPR;
   for (int i = threadIdx.x * 16; i < TILE; i += NT * 16)
     *reinterpret_cast<uint4*>(mark + i) = make_uint4(0, 0, 0, 0);
+  if (threadIdx.x == 0) nborder = 0;
   const int nval = max(0, min(PX, t.tw - xl));
   const unsigned vmask = (1u << nval) - 1u;
   const bool vec = g.vec_img && nval == PX;
@@ -469,7 +486,21 @@ __global__ void __launch_bounds__(NT) k_tile_local(const T* __restrict__ img, ui
   }
   __syncthreads();
 
-  // ---- global parent slots for leaders whose region touches the border
+  // ---- border records: colour and leader of the left and right columns
+  uint32_t* rec = bd.rec + (long long)blockIdx.x * 4 * TH;
+  if (threadIdx.x < 2 * t.th) {
+    const int r = threadIdx.x % t.th, right = threadIdx.x / t.th;
+    const int i = r * TW + (right ? t.tw - 1 : 0);
+    const int p = par[i];
+    const int lead = p < 0 ? -1 : find_s(par, i, cap, status);
+    rec[2 * right * TH + r] = (uint32_t)col[i];
+    rec[(2 * right + 1) * TH + r] =
+        lead < 0 ? 0xFFFFFFFFu : (uint32_t)((t.y0 + (lead >> LOG_TW)) * g.W + t.x0 + (lead & (TW - 1)));
+  }
+
+  // ---- leaders whose region touches the border: a global parent slot and
+  // an entry in the tile's border list
+  uint16_t* blist = bd.list + (long long)blockIdx.x * BLCAP;
 #pragma unroll
   for (int k = 0; k < RPW; ++k) {
     const int r = warp + k * NWARPS;
@@ -477,49 +508,31 @@ __global__ void __launch_bounds__(NT) k_tile_local(const T* __restrict__ img, ui
     while (m) {
       const int j = __ffs(m) - 1;
       m &= m - 1;
-      if (mark[r * TW + xl + j]) {
+      const int i = r * TW + xl + j;
+      if (mark[i]) {
         const int gi = (t.y0 + r) * g.W + t.x0 + xl + j;
         Pi[gi] = gi;
+        const int slot = atomicAdd(&nborder, 1);
+        if (slot < BLCAP) blist[slot] = (uint16_t)i;
       }
     }
   }
+  __syncthreads();
+  if (threadIdx.x == 0) bd.cnt[blockIdx.x] = (uint32_t)min(nborder, BLCAP);
 }
 
-// The joins of pixel (y, x) -- the same rule as inside a tile, on the true
-// neighbourhood -- whose partner lies outside the pixel's tile.
-template <typename T, int CONN, bool BIN>
-__device__ __forceinline__ void seam_joins(const T* __restrict__ im, const uint16_t* __restrict__ Li,
-                                           int32_t* P, uint32_t* bm, uint32_t* cnt, const Geom& g,
-                                           int y, int x, int y0, int x0, int cap, int* status) {
-  const long long row = (long long)y * g.W;
-  const T c = im[row + x];
-  if (BIN && c == 0) return;
-  const bool hasU = y > 0, hasL = x > 0;
-  const bool eqL = hasL && im[row + x - 1] == c;
-  const bool eqU = hasU && im[row - g.W + x] == c;
-  const bool eqUL = hasU && hasL && im[row - g.W + x - 1] == c;
-  const bool eqUR = (CONN == 8) && hasU && x + 1 < g.W && im[row - g.W + x + 1] == c;
-  int a = -1;
-  auto join = [&](int qy, int qx) {
-    if (qy >= y0 && qx >= x0 && qx < x0 + TW) return;   // inside the tile
-    if (a < 0) a = leader_of(Li, y, x, g);
-    const int bq = leader_of(Li, qy, qx, g);
-    union_g(P, a, bq, bm, cnt, g, cap, status);
-  };
-  if (CONN == 8) {
-    if (eqU && !eqL) join(y - 1, x);
-    if (eqUL && !eqU && !eqL) join(y - 1, x - 1);
-    if (eqUR && !eqU) join(y - 1, x + 1);
-  } else {
-    if (eqU && !(eqL && eqUL)) join(y - 1, x);
-  }
-  if (eqL) join(y, x - 1);
-}
-
+// Connect across tile seams: the joins of the same rule as inside a tile,
+// evaluated on the true neighbourhood, whose partner lies in another tile.
+// A tile handles its top seam (its first row against the row above, read
+// whole and coalesced) and its left seam (its left column against the left
+// tile's right column, from the border records).
 template <typename T, int CONN, bool BIN>
 __global__ void __launch_bounds__(NT) k_seams(const T* __restrict__ img, const uint16_t* __restrict__ L16,
-                                              int32_t* P, uint32_t* bm, uint32_t* cnt, Geom g, int cap,
-                                              int* status) {
+                                              int32_t* P, uint32_t* bm, uint32_t* cnt, Border bd,
+                                              Geom g, int cap, int* status) {
+  static_assert(NT == TW, "one thread per column of the tile");
+  __shared__ uint32_t cc[TW + 2], ca[TW + 2];   // rows y0 and y0-1, columns x0-1 .. x0+TW
+  __shared__ uint16_t lc[TW], la[TW];           // leader map of the same rows
   const TileCoord t = tile_coord(g);
   const long long ioff = (long long)t.b * g.HW;
   const T* im = img + ioff;
@@ -527,13 +540,88 @@ __global__ void __launch_bounds__(NT) k_seams(const T* __restrict__ img, const u
   int32_t* Pi = P + ioff;
   uint32_t* bmi = bm + (long long)t.b * g.H * g.WPR;
   uint32_t* cnti = cnt + (long long)t.b * g.H * g.CPR;
-  const int nTop = t.tw, nSide = t.th - 1;
-  for (int k = threadIdx.x; k < nTop + 2 * nSide; k += NT) {
-    int y, x;
-    if (k < nTop) { y = t.y0; x = t.x0 + k; }
-    else if (k < nTop + nSide) { y = t.y0 + 1 + (k - nTop); x = t.x0; }
-    else { y = t.y0 + 1 + (k - nTop - nSide); x = t.x0 + t.tw - 1; }
-    seam_joins<T, CONN, BIN>(im, Li, Pi, bmi, cnti, g, y, x, t.y0, t.x0, cap, status);
+  const int x = threadIdx.x;
+  const bool top = t.y0 > 0;
+  const long long row = (long long)t.y0 * g.W + t.x0;
+  if (x < t.tw) {
+    cc[x + 1] = im[row + x];
+    lc[x] = Li[row + x];
+    if (top) {
+      ca[x + 1] = im[row - g.W + x];
+      la[x] = Li[row - g.W + x];
+    }
+  }
+  if (x == 0 && t.x0 > 0) {
+    cc[0] = im[row - 1];
+    if (top) ca[0] = im[row - g.W - 1];
+  }
+  if (x == 1 && t.x0 + t.tw < g.W) {
+    cc[t.tw + 1] = im[row + t.tw];
+    if (top) ca[t.tw + 1] = im[row - g.W + t.tw];
+  }
+  __syncthreads();
+  const int n = (int)g.HW;
+
+  // ---- top row of the tile
+  if (x < t.tw) {
+    const uint32_t c = cc[x + 1];
+    if (!(BIN && c == 0)) {
+      const bool hasL = t.x0 + x > 0, hasR = t.x0 + x + 1 < g.W;
+      const bool eqL = hasL && cc[x] == c;
+      const bool eqU = top && ca[x + 1] == c;
+      const bool eqUL = top && hasL && ca[x] == c;
+      const bool eqUR = (CONN == 8) && top && hasR && ca[x + 2] == c;
+      // this pixel's leader: the map gives its run start (in this row), whose
+      // entry gives the leader; a run start's own entry already is the leader
+      const int l1 = lc[x], l2 = (l1 >> LOG_TW) == 0 ? lc[l1 & (TW - 1)] : l1;
+      const int a = (t.y0 + (l2 >> LOG_TW)) * g.W + t.x0 + (l2 & (TW - 1));
+      auto up = [&](int d) {
+        const int xx = x + d;
+        int b;
+        if (xx >= 0 && xx < t.tw) {   // the tile above: its last row is row y0-1
+          const int m1 = la[xx], m2 = (m1 >> LOG_TW) == TH - 1 ? la[m1 & (TW - 1)] : m1;
+          b = (t.y0 - TH + (m2 >> LOG_TW)) * g.W + t.x0 + (m2 & (TW - 1));
+        } else {
+          b = leader_of(Li, t.y0 - 1, t.x0 + xx, g);
+        }
+        if (b >= 0 && b < n) union_g(Pi, a, b, bmi, cnti, g, cap, status);
+      };
+      if (CONN == 8) {
+        if (eqU && !eqL) up(0);
+        if (eqUL && !eqU && !eqL) up(-1);
+        if (eqUR && !eqU) up(1);
+      } else {
+        if (eqU && !(eqL && eqUL)) up(0);
+      }
+      if (eqL && x == 0) {   // left neighbour in the left tile: its border record
+        const int b = (int)bd.rec[((long long)blockIdx.x - 1) * 4 * TH + 3 * TH];
+        if (b >= 0 && b < n) union_g(Pi, a, b, bmi, cnti, g, cap, status);
+      }
+    }
+  }
+
+  // ---- left column of the tile (rows below the first) against the left
+  // tile's right column
+  if (t.x0 > 0 && x >= 1 && x < t.th) {
+    const int r = x;
+    const uint32_t* recT = bd.rec + (long long)blockIdx.x * 4 * TH;
+    const uint32_t* recL = recT - 4 * TH;
+    const uint32_t cp = recT[r], cU = recT[r - 1];                     // (r, x0), (r-1, x0)
+    const uint32_t cq = recL[2 * TH + r], cUL = recL[2 * TH + r - 1];  // (r, x0-1), (r-1, x0-1)
+    const int lp = (int)recT[TH + r], lU = (int)recT[TH + r - 1];
+    const int lq = (int)recL[3 * TH + r], lUL = (int)recL[3 * TH + r - 1];
+    const bool fgp = !BIN || cp != 0, fgq = !BIN || cq != 0;
+    const bool eqL = fgp && cp == cq;
+    auto join = [&](int a, int b) {
+      if (a >= 0 && a < n && b >= 0 && b < n) union_g(Pi, a, b, bmi, cnti, g, cap, status);
+    };
+    if (eqL) join(lp, lq);
+    if (CONN == 8) {
+      const bool eqU = cp == cU, eqUL = fgp && cp == cUL;
+      if (eqUL && !eqU && !eqL) join(lp, lUL);
+      // (r, x0-1) joins its up-right (r-1, x0) unless its own up matches
+      if (fgq && cq == cU && cq != cUL) join(lq, lU);
+    }
   }
 }
 
@@ -637,33 +725,30 @@ __device__ __forceinline__ int number_of(int gidx, const uint32_t* bmi, const ui
   return (int)(offi[(long long)gy * g.CPR + (gx >> LOG_TW)] - base0 + s + 1u);
 }
 
-// Collapse + Number for the leaders re-pointed across seams.  Every such
-// leader's tile region touches the tile border, so starting from the border
-// pixels reaches all of them.  Each walks to its final leader (halving on
-// the way), takes that leader's label, and stores it negated in its own
-// slot.  A walk that meets a slot already holding a negated label stops
-// there: every node on a walk belongs to the same region.
-__global__ void __launch_bounds__(NT) k_resolve(const uint16_t* __restrict__ L16, int32_t* P,
+// Collapse + Number for the leaders re-pointed across seams, taken from the
+// tiles' border lists (a warp per tile).  Each walks to its final leader
+// (halving on the way), takes that leader's label and stores it negated in
+// its own slot.  A walk that meets a slot already holding a negated label
+// stops there: every node on a walk belongs to the same region.
+__global__ void __launch_bounds__(NT) k_resolve(Border bd, long long nTiles, int32_t* P,
                                                 const uint32_t* __restrict__ bm,
                                                 const uint32_t* __restrict__ off, Geom g, int cap,
                                                 int* status) {
-  const TileCoord t = tile_coord(g);
+  const long long tile = (long long)blockIdx.x * NWARPS + (threadIdx.x >> 5);
+  if (tile >= nTiles) return;
+  const int lane = threadIdx.x & 31;
+  const TileCoord t = tile_coord_of(g, tile);
   const long long ioff = (long long)t.b * g.HW;
-  const uint16_t* Li = L16 + ioff;
   int32_t* Pi = P + ioff;
   const uint32_t* bmi = bm + (long long)t.b * g.H * g.WPR;
   const uint32_t* offi = off + (long long)t.b * g.H * g.CPR;
   const uint32_t base0 = offi[0];
   const int n = (int)g.HW;
-  const int np = 2 * t.tw + 2 * t.th;
-  for (int k = threadIdx.x; k < np; k += NT) {
-    int y, x;
-    if (k < t.tw) { y = t.y0; x = t.x0 + k; }
-    else if (k < 2 * t.tw) { y = t.y0 + t.th - 1; x = t.x0 + (k - t.tw); }
-    else if (k < 2 * t.tw + t.th) { y = t.y0 + (k - 2 * t.tw); x = t.x0; }
-    else { y = t.y0 + (k - 2 * t.tw - t.th); x = t.x0 + t.tw - 1; }
-    const int r = leader_of(Li, y, x, g);
-    if (r < 0) continue;
+  const int count = min((int)bd.cnt[tile], BLCAP);
+  const uint16_t* list = bd.list + tile * BLCAP;
+  for (int k = lane; k < count; k += 32) {
+    const int l = list[k];
+    const int r = (t.y0 + (l >> LOG_TW)) * g.W + t.x0 + (l & (TW - 1));
     const int v = __ldcg(Pi + r);
     if (v == r || v < 0) continue;   // still a leader, or already resolved
     int node = r, lab = 0, s = 0;
