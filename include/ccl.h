@@ -164,8 +164,8 @@ long long ccl_kernel_launches(void);
  * held by every GPU that loads the library until the process exits; 256
  * bytes of it are a status word and the rest must be at least
  * ccl_workspace_bytes(...) for these arguments, else the call returns
- * CCL_ERR_TOO_LARGE without doing anything (about 2.1 bytes per pixel:
- * roughly 15 million pixels per call).
+ * CCL_ERR_TOO_LARGE without doing anything (about 2.5 bytes per pixel:
+ * roughly 13 million pixels per call).
  *  - The first call on a device looks up the array's device address (with
  *    that device current) and caches it; make that first call before any
  *    stream capture.
