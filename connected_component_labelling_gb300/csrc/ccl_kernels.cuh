@@ -533,6 +533,12 @@ __global__ void __launch_bounds__(NT) k_seams(const T* __restrict__ img, const u
   static_assert(NT == TW, "one thread per column of the tile");
   __shared__ uint32_t cc[TW + 2], ca[TW + 2];   // rows y0 and y0-1, columns x0-1 .. x0+TW
   __shared__ uint16_t lc[TW], la[TW];           // leader map of the same rows
+  // pairs of leaders already joined by this tile: many joins along a seam
+  // link the same two regions, and only the first needs a global union
+  constexpr int HSIZE = 2 * NT;
+  constexpr unsigned long long EMPTY = ~0ull;
+  __shared__ unsigned long long seen[HSIZE];
+  for (int i = threadIdx.x; i < HSIZE; i += NT) seen[i] = EMPTY;
   const TileCoord t = tile_coord(g);
   const long long ioff = (long long)t.b * g.HW;
   const T* im = img + ioff;
@@ -561,6 +567,19 @@ __global__ void __launch_bounds__(NT) k_seams(const T* __restrict__ img, const u
   }
   __syncthreads();
   const int n = (int)g.HW;
+  auto join_once = [&](int a, int b) {
+    if (a == b || a < 0 || b < 0 || a >= n || b >= n) return;
+    const unsigned long long key =
+        ((unsigned long long)(unsigned)min(a, b) << 32) | (unsigned)max(a, b);
+    unsigned h = (unsigned)((key * 0x9E3779B97F4A7C15ull) >> 40) & (HSIZE - 1);
+    for (int probe = 0; probe < 8; ++probe) {
+      const unsigned long long prev = atomicCAS(&seen[h], EMPTY, key);
+      if (prev == key) return;                 // joined already by this tile
+      if (prev == EMPTY) break;                // first time: join it
+      h = (h + 1) & (HSIZE - 1);
+    }
+    union_g(Pi, a, b, bmi, cnti, g, cap, status);
+  };
 
   // ---- top row of the tile
   if (x < t.tw) {
@@ -584,7 +603,7 @@ __global__ void __launch_bounds__(NT) k_seams(const T* __restrict__ img, const u
         } else {
           b = leader_of(Li, t.y0 - 1, t.x0 + xx, g);
         }
-        if (b >= 0 && b < n) union_g(Pi, a, b, bmi, cnti, g, cap, status);
+        join_once(a, b);
       };
       if (CONN == 8) {
         if (eqU && !eqL) up(0);
@@ -594,8 +613,7 @@ __global__ void __launch_bounds__(NT) k_seams(const T* __restrict__ img, const u
         if (eqU && !(eqL && eqUL)) up(0);
       }
       if (eqL && x == 0) {   // left neighbour in the left tile: its border record
-        const int b = (int)bd.rec[((long long)blockIdx.x - 1) * 4 * TH + 3 * TH];
-        if (b >= 0 && b < n) union_g(Pi, a, b, bmi, cnti, g, cap, status);
+        join_once(a, (int)bd.rec[((long long)blockIdx.x - 1) * 4 * TH + 3 * TH]);
       }
     }
   }
@@ -612,15 +630,12 @@ __global__ void __launch_bounds__(NT) k_seams(const T* __restrict__ img, const u
     const int lq = (int)recL[3 * TH + r], lUL = (int)recL[3 * TH + r - 1];
     const bool fgp = !BIN || cp != 0, fgq = !BIN || cq != 0;
     const bool eqL = fgp && cp == cq;
-    auto join = [&](int a, int b) {
-      if (a >= 0 && a < n && b >= 0 && b < n) union_g(Pi, a, b, bmi, cnti, g, cap, status);
-    };
-    if (eqL) join(lp, lq);
+    if (eqL) join_once(lp, lq);
     if (CONN == 8) {
       const bool eqU = cp == cU, eqUL = fgp && cp == cUL;
-      if (eqUL && !eqU && !eqL) join(lp, lUL);
+      if (eqUL && !eqU && !eqL) join_once(lp, lUL);
       // (r, x0-1) joins its up-right (r-1, x0) unless its own up matches
-      if (fgq && cq == cU && cq != cUL) join(lq, lU);
+      if (fgq && cq == cU && cq != cUL) join_once(lq, lU);
     }
   }
 }

@@ -55,8 +55,45 @@ def _load():
                 ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
                 ctypes.c_int, ctypes.c_int, ctypes.c_int,
                 ctypes.c_void_p, ctypes.c_void_p]
+            lib.oracle_label_ignore.restype = ctypes.c_int
+            lib.oracle_label_ignore.argtypes = [
+                ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
+                ctypes.c_void_p, ctypes.c_void_p]
             _lib = lib
     return _lib
+
+
+def _shape(a):
+    if a.dtype == np.uint8 and a.ndim == 4:      # [B,H,W,pixel_bytes]
+        B, H, W, pb = a.shape
+        return B, H, W, pb, False
+    if a.ndim == 3:
+        B, H, W = a.shape
+        return B, H, W, a.dtype.itemsize, False
+    if a.ndim == 2:
+        H, W = a.shape
+        return 1, H, W, a.dtype.itemsize, True
+    raise ValueError("expected a [B,]H,W array")
+
+
+def label_ignore(img: np.ndarray, ignore_value: int, connectivity: int = 8):
+    """Like ``label`` in the all-pixels mode, but pixels equal to
+    ``ignore_value`` (an integer holding the pixel's bytes, little-endian)
+    are background: label 0, joining nothing ("every-colour", ch. 08
+    switch 4)."""
+    a = np.ascontiguousarray(img)
+    B, H, W, pb, squeeze = _shape(a)
+    ign = np.frombuffer(int(ignore_value).to_bytes(8, "little")[:pb], dtype=np.uint8).copy()
+    labels = np.empty((B, H, W), dtype=np.int32)
+    n = np.empty((B,), dtype=np.int32)
+    rc = _load().oracle_label_ignore(a.ctypes.data, B, H, W, pb, connectivity, ign.ctypes.data,
+                                     labels.ctypes.data, n.ctypes.data)
+    if rc != 0:
+        raise RuntimeError("oracle_label_ignore failed with status %d" % rc)
+    if squeeze:
+        return labels[0], n[0]
+    return labels, n
 
 
 def label(img: np.ndarray, connectivity: int = 8, mode: int = MODE_ALL):

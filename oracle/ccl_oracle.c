@@ -55,7 +55,8 @@ static int is_zero(const uint8_t* a, int pb) {
  * number of regions.
  */
 static int64_t label_one(const uint8_t* img, int64_t H, int64_t W, int pb,
-                         int conn, int mode, int32_t* labels, int64_t* queue) {
+                         int conn, int mode, const uint8_t* ign,
+                         int32_t* labels, int64_t* queue) {
   const int64_t N = H * W;
   /* neighbour offsets: 4-connectivity uses the first four (edge-sharing),
    * 8-connectivity adds the four corner-sharing ones */
@@ -69,6 +70,8 @@ static int64_t label_one(const uint8_t* img, int64_t H, int64_t W, int pb,
     const uint8_t* v = img + i * pb;
     if (mode == ORACLE_MODE_BINARY && is_zero(v, pb))
       labels[i] = 0;
+    else if (ign && same_value(v, ign, pb))
+      labels[i] = 0;   /* the ignored value: background */
     else
       labels[i] = -1;
   }
@@ -105,9 +108,36 @@ static int64_t label_one(const uint8_t* img, int64_t H, int64_t W, int pb,
  * Host pointers only.  Returns ORACLE_OK, ORACLE_ERR_INVALID_ARG or
  * ORACLE_ERR_NO_MEMORY.
  */
+static int label_all(const void* img, int64_t batch, int64_t H, int64_t W,
+                     int pixel_bytes, int connectivity, int mode,
+                     const uint8_t* ign, int32_t* labels, int32_t* n_out);
+
 int oracle_label(const void* img, int64_t batch, int64_t H, int64_t W,
                  int pixel_bytes, int connectivity, int mode,
                  int32_t* labels, int32_t* n_out) {
+  return label_all(img, batch, H, W, pixel_bytes, connectivity, mode, NULL,
+                   labels, n_out);
+}
+
+/*
+ * oracle_label_ignore: as oracle_label in the all-pixels mode, except that
+ * pixels whose pixel_bytes bytes equal ignore_value (host pointer to
+ * pixel_bytes bytes) are background: label 0, joining nothing
+ * ("every-colour", ch. 08 switch 4 "Ignore the paper": the named colour
+ * gets label 0 and takes part in nothing after).
+ */
+int oracle_label_ignore(const void* img, int64_t batch, int64_t H, int64_t W,
+                        int pixel_bytes, int connectivity,
+                        const void* ignore_value, int32_t* labels,
+                        int32_t* n_out) {
+  if (!ignore_value) return ORACLE_ERR_INVALID_ARG;
+  return label_all(img, batch, H, W, pixel_bytes, connectivity, ORACLE_MODE_ALL,
+                   (const uint8_t*)ignore_value, labels, n_out);
+}
+
+static int label_all(const void* img, int64_t batch, int64_t H, int64_t W,
+                     int pixel_bytes, int connectivity, int mode,
+                     const uint8_t* ign, int32_t* labels, int32_t* n_out) {
   if (batch < 0 || H < 0 || W < 0) return ORACLE_ERR_INVALID_ARG;
   if (pixel_bytes < 1 || pixel_bytes > 16) return ORACLE_ERR_INVALID_ARG;
   if (connectivity != 4 && connectivity != 8) return ORACLE_ERR_INVALID_ARG;
@@ -125,7 +155,7 @@ int oracle_label(const void* img, int64_t batch, int64_t H, int64_t W,
   const uint8_t* base = (const uint8_t*)img;
   for (int64_t b = 0; b < batch; ++b) {
     n_out[b] = (int32_t)label_one(base + b * N * pixel_bytes, H, W,
-                                  pixel_bytes, connectivity, mode,
+                                  pixel_bytes, connectivity, mode, ign,
                                   labels + b * N, queue);
   }
   free(queue);

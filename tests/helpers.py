@@ -68,7 +68,7 @@ def _neighbour_offsets(conn):
     return [(dr, dc) for dr in (-1, 0, 1) for dc in (-1, 0, 1) if (dr, dc) != (0, 0)]
 
 
-def closure_labels(imgs, conn, binary):
+def closure_labels(imgs, conn, binary, ignore=None):
     """Brute force for a batch of tiny images [B,H,W] (H*W <= 64).
 
     Builds the adjacency matrix of the pixel graph (neighbours of equal value,
@@ -80,7 +80,9 @@ def closure_labels(imgs, conn, binary):
     B, H, W = imgs.shape
     N = H * W
     flat = imgs.reshape(B, N)
-    active = (flat != 0) if binary else np.ones_like(flat, dtype=bool)
+    if binary:
+        ignore = 0
+    active = (flat != ignore) if ignore is not None else np.ones_like(flat, dtype=bool)
     A = np.zeros((B, N, N), dtype=np.float32)
     idx = np.arange(N)
     A[:, idx, idx] = active
@@ -106,7 +108,7 @@ def closure_labels(imgs, conn, binary):
     return lab.reshape(B, H, W), is_first.sum(axis=1)
 
 
-def scipy_labels(img, conn, binary):
+def scipy_labels(img, conn, binary, ignore=None):
     """Partition via scipy.ndimage.label run once per distinct value,
     then renumbered canonically.  Returns (labels, n)."""
     from scipy import ndimage
@@ -114,14 +116,16 @@ def scipy_labels(img, conn, binary):
     structure = ndimage.generate_binary_structure(2, 1 if conn == 4 else 2)
     out = np.zeros(img.shape, dtype=np.int64)
     nxt = 0
+    if binary:
+        ignore = 0
     for v in np.unique(img):
-        if binary and v == 0:
+        if ignore is not None and v == ignore:
             continue
         lab, k = ndimage.label(img == v, structure=structure)
         m = lab > 0
         out[m] = lab[m] + nxt
         nxt += k
-    bg = (img == 0) if binary else None
+    bg = (img == ignore) if ignore is not None else None
     return canonicalize(out, bg)
 
 

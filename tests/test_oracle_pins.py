@@ -279,3 +279,63 @@ def test_pins_catch_planted_mistakes(tmp_path, key):
     lab, n = _run(lib, img, 8, 0)
     caught |= int(n[0]) != 2
     assert caught, key
+
+
+# ------------------------------------------------------ ignoring one value
+# "every-colour", ch. 08 switch 4 "Ignore the paper": pixels of the named
+# value get label 0 and take part in nothing.
+
+@pytest.mark.parametrize("conn", [4, 8])
+@pytest.mark.parametrize("ignore", [0, 1, 2])
+def test_ignore_bruteforce_all_3colour_3x3(conn, ignore):
+    imgs = np.array(list(itertools.product(range(3), repeat=9)), dtype=np.uint8).reshape(-1, 3, 3)
+    lab, n = oracle.label_ignore(imgs, ignore, conn)
+    bl, bn = closure_labels(imgs, conn, False, ignore=ignore)
+    np.testing.assert_array_equal(lab, bl)
+    np.testing.assert_array_equal(n, bn)
+
+
+@pytest.mark.parametrize("conn", [4, 8])
+def test_ignore_zero_is_binary_mode(conn):
+    rng = np.random.default_rng(7)
+    imgs = rng.integers(0, 4, size=(3, 41, 67)).astype(np.uint8)
+    a, na = oracle.label_ignore(imgs, 0, conn)
+    b, nb = oracle.label(imgs, conn, oracle.MODE_BINARY)
+    np.testing.assert_array_equal(a, b)
+    np.testing.assert_array_equal(na, nb)
+
+
+@pytest.mark.parametrize("conn", [4, 8])
+def test_ignore_white_on_rgba_against_scipy(conn):
+    import workloads
+    img = workloads.drawing(150, 230, seed=3, n_segments=40, n_rects=5, levels=16,
+                            hatched=False).numpy().view(np.uint32)
+    lab, n = oracle.label_ignore(img, 0xFFFFFFFF, conn)
+    sl, sn = scipy_labels(img, conn, False, ignore=0xFFFFFFFF)
+    np.testing.assert_array_equal(lab, sl)
+    assert n == sn
+    assert (lab[img == 0xFFFFFFFF] == 0).all()
+
+
+def test_ignore_compares_every_byte(tmp_path):
+    # a copy that compares only the first byte against the ignored value
+    # must fail this pin: 0x7FFFFFFF differs from white only in alpha
+    img = np.full((2, 3), 0x7FFFFFFF, np.uint32)
+    lab, n = oracle.label_ignore(img, 0xFFFFFFFF, 8)
+    assert n == 1 and (lab == 1).all()
+    src = open(oracle._SRC).read()
+    old = "else if (ign && same_value(v, ign, pb))"
+    assert old in src
+    path = tmp_path / "m_ign.c"
+    path.write_text(src.replace(old, "else if (ign && v[0] == ign[0])", 1))
+    so = tmp_path / "m_ign.so"
+    subprocess.check_call(["gcc", "-O1", "-std=c99", "-shared", "-fPIC", "-o", str(so), str(path)])
+    import ctypes
+    lib = ctypes.CDLL(str(so))
+    ign = np.frombuffer((0xFFFFFFFF).to_bytes(4, "little"), np.uint8).copy()
+    out = np.empty((1, 2, 3), np.int32)
+    cnt = np.empty(1, np.int32)
+    lib.oracle_label_ignore(ctypes.c_void_p(img.ctypes.data), ctypes.c_int64(1), ctypes.c_int64(2),
+                            ctypes.c_int64(3), 4, 8, ctypes.c_void_p(ign.ctypes.data),
+                            ctypes.c_void_p(out.ctypes.data), ctypes.c_void_p(cnt.ctypes.data))
+    assert cnt[0] != 1          # the planted mistake is caught
