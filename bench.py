@@ -50,6 +50,11 @@ def make_workload(name, device):
         img = wl.c4_sheet(device=device)
         return (dict(workload="c4_sheet_24000x33600_rgba", batch=1, H=wl.C4_H, W=wl.C4_W,
                      pixel_bytes=4, connectivity=8, mode="all"), img, 4, 8, 0)
+    if name == "c4i":               # the sheet with its white paper ignored
+        img = wl.c4_sheet(device=device)
+        return (dict(workload="c4_sheet_24000x33600_rgba_paper_ignored", batch=1, H=wl.C4_H,
+                     W=wl.C4_W, pixel_bytes=4, connectivity=8, mode="ignore",
+                     ignore_value="0xFFFFFFFF"), img, 4, 8, -1)
     if name.startswith("c4:"):      # the sheet generator at another size, e.g. c4:6000x8400
         H, W = (int(v) for v in name[3:].split("x"))
         img = wl.c4_sheet(device=device, H=H, W=W)
@@ -283,16 +288,21 @@ def main():
     px = B * H * W
     labels = torch.empty(px, dtype=torch.int32, device=dev)
     nreg = torch.empty(B, dtype=torch.int32, device=dev)
-    wsb = ccl.ccl_workspace_bytes(B, H, W, pb, conn, mode)
+    wsb = ccl.ccl_workspace_bytes(B, H, W, pb, conn, max(mode, 0))
     ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     sp = stream.cuda_stream
 
     def step():
-        rc = ccl.ccl_label_ws(img.data_ptr(), B, H, W, pb, conn, mode, labels.data_ptr(),
-                              nreg.data_ptr(), ws.data_ptr(), wsb, sp)
+        if mode < 0:   # one value ignored
+            rc = ccl.ccl_label_ignore(img.data_ptr(), B, H, W, pb, conn,
+                                      int(cfg["ignore_value"], 16), labels.data_ptr(),
+                                      nreg.data_ptr(), ws.data_ptr(), wsb, sp)
+        else:
+            rc = ccl.ccl_label_ws(img.data_ptr(), B, H, W, pb, conn, mode, labels.data_ptr(),
+                                  nreg.data_ptr(), ws.data_ptr(), wsb, sp)
         if rc != ccl.CCL_OK:
-            raise ccl.CCLError(rc, "ccl_label_ws")
+            raise ccl.CCLError(rc, "labelling call")
 
     for _ in range(args.warmup):
         step()
@@ -381,7 +391,7 @@ def main():
 
     # ---- e2e through the host entry point
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and mode >= 0:
         himg = img.cpu().contiguous().pin_memory()
         hlab = torch.empty(px, dtype=torch.int32).pin_memory()
         hn = torch.empty(B, dtype=torch.int32).pin_memory()
@@ -412,7 +422,12 @@ def main():
         import oracle
         oracle.build()
         band = img[:CPU_BASELINE_ROWS].cpu().numpy().view(np.uint32)
-        dt = time_oracle(band, 8, oracle.MODE_ALL)
+        if mode < 0:
+            t0 = time.perf_counter()
+            oracle.label_ignore(band, int(cfg["ignore_value"], 16), 8)
+            dt = time.perf_counter() - t0
+        else:
+            dt = time_oracle(band, 8, oracle.MODE_ALL)
         cpu_baseline = {"value": band.size / dt / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
                         "sample": "rows 0-%d of the sheet (%d px), one single-threaded BFS pass, "
                                   "%.1f s" % (CPU_BASELINE_ROWS, band.size, dt)}

@@ -31,7 +31,8 @@ CCL_OPT_STAGE_EVENTS = 2
 # every symbol include/ccl.h declares
 EXPORTED = ("ccl_label", "ccl_workspace_bytes", "ccl_label_ws", "ccl_label_host",
             "ccl_last_status", "ccl_status_string", "ccl_set_option", "ccl_stage_times",
-            "ccl_stage_name", "ccl_kernel_launches", "ccl_label_noalloc", "ccl_version")
+            "ccl_stage_name", "ccl_kernel_launches", "ccl_label_noalloc", "ccl_label_ignore",
+            "ccl_version")
 
 _lock = threading.Lock()
 _lib = None
@@ -75,6 +76,9 @@ def lib():
             L.ccl_kernel_launches.restype = ctypes.c_longlong
             L.ccl_label_noalloc.argtypes = [vp, i32, i32, i32, i32, i32, i32, vp, vp, vp]
             L.ccl_label_noalloc.restype = i32
+            L.ccl_label_ignore.argtypes = [vp, i32, i32, i32, i32, i32, ctypes.c_uint32, vp, vp,
+                                           vp, sz, vp]
+            L.ccl_label_ignore.restype = i32
             L.ccl_version.argtypes = []
             L.ccl_version.restype = i32
             _lib = L
@@ -144,6 +148,40 @@ def ccl_label_noalloc(img, batch, H, W, pixel_bytes, connectivity, mode, labels,
 
 
 CCL_NOALLOC_SCRATCH_BYTES = 32 << 20
+
+
+def ccl_label_ignore(img, batch, H, W, pixel_bytes, connectivity, ignore_value, labels,
+                     n_regions, workspace, workspace_bytes, stream):
+    return lib().ccl_label_ignore(img, batch, H, W, pixel_bytes, connectivity, ignore_value,
+                                  labels, n_regions, workspace, workspace_bytes, stream)
+
+
+def label_ignore(img, ignore_value, connectivity=8, out=None, n_out=None, workspace=None,
+                 stream=None):
+    """Label a CUDA tensor of images with pixels equal to ``ignore_value``
+    (the pixel's bytes as a little-endian integer) as background: label 0,
+    joining nothing.  Returns (labels, n_regions) like ``label``."""
+    import torch
+    if not img.is_cuda:
+        raise ValueError("label_ignore() needs a CUDA tensor; the library has no CPU path")
+    img = img.contiguous()
+    B, H, W, pb, squeeze = image_geometry(img)
+    if out is None:
+        out = torch.empty((B, H, W), dtype=torch.int32, device=img.device)
+    if n_out is None:
+        n_out = torch.empty((B,), dtype=torch.int32, device=img.device)
+    st = stream if stream is not None else torch.cuda.current_stream(img.device)
+    wp, wb = (workspace.data_ptr(), workspace.numel() * workspace.element_size()) \
+        if workspace is not None else (None, 0)
+    with torch.cuda.device(img.device):
+        rc = ccl_label_ignore(img.data_ptr(), B, H, W, pb, connectivity,
+                              int(ignore_value) & 0xFFFFFFFF, out.data_ptr(), n_out.data_ptr(),
+                              wp, wb, st.cuda_stream)
+    if rc != CCL_OK:
+        raise CCLError(rc, "ccl_label_ignore")
+    if squeeze:
+        return out.view(H, W), n_out.view(())
+    return out, n_out
 
 
 def ccl_version():

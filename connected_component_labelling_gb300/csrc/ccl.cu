@@ -208,8 +208,8 @@ void k_seams_dispatch(int pb, int conn, int mode, const void* img, const uint16_
 // `status` the device word the kernels flag limits in, `events` whether the
 // optional per-stage events may be recorded.
 int run_pipeline(const void* img, int batch, int H, int W, int pb, int conn, int mode,
-                 int32_t* labels, int32_t* n_out, const Layout& L, void* ws, int* status,
-                 bool events, cudaStream_t st) {
+                 uint32_t bgval, int32_t* labels, int32_t* n_out, const Layout& L, void* ws,
+                 int* status, bool events, cudaStream_t st) {
   char* base = (char*)ws;
   uint16_t* L16 = (uint16_t*)(base + L.offL16);
   uint32_t* bm = (uint32_t*)(base + L.offBm);
@@ -234,6 +234,7 @@ int run_pipeline(const void* img, int batch, int H, int W, int pb, int conn, int
   };
   // vector access when every row start keeps the needed alignment
   Geom g = L.g;
+  g.bgval = bgval;
   const uintptr_t ia = (uintptr_t)img;
   if (pb == 1) g.vec_img = (W % 8 == 0) && (ia % 8 == 0);
   else if (pb == 2) g.vec_img = (W % 8 == 0) && (ia % 16 == 0);
@@ -262,11 +263,14 @@ int run_pipeline(const void* img, int batch, int H, int W, int pb, int conn, int
 }
 
 int run(const void* img, int batch, int H, int W, int pb, int conn, int mode, int32_t* labels,
-        int32_t* n_out, const Layout& L, void* ws, cudaStream_t st) {
+        int32_t* n_out, const Layout& L, void* ws, cudaStream_t st, uint32_t bgval = 0u) {
   int* status = nullptr;
   int rc = device_status_ptr(&status);
   if (rc != CCL_OK) return rc;
-  return run_pipeline(img, batch, H, W, pb, conn, mode, labels, n_out, L, ws, status, true, st);
+  if (bgval != 0u)
+    return run_pipeline(img, batch, H, W, pb, conn, mode, bgval, labels, n_out, L, ws, status,
+                        true, st);
+  return run_pipeline(img, batch, H, W, pb, conn, mode, 0u, labels, n_out, L, ws, status, true, st);
 }
 
 int empty_call(int batch, int32_t* n_out, cudaStream_t st) {
@@ -386,6 +390,45 @@ int ccl_label(const void* img, int batch, int H, int W, int pixel_bytes, int con
     return CCL_ERR_NO_MEMORY;
   }
   rc = run(img, batch, H, W, pixel_bytes, connectivity, mode, labels_i32, n_regions_out, L, ws, st);
+  if (cudaFreeAsync(ws, st) != cudaSuccess && rc == CCL_OK) rc = CCL_ERR_CUDA;
+  return rc;
+}
+
+int ccl_label_ignore(const void* img, int batch, int H, int W, int pixel_bytes, int connectivity,
+                     uint32_t ignore_value, int32_t* labels_i32, int32_t* n_regions_out,
+                     void* workspace, size_t workspace_bytes, ccl_stream_t stream) {
+  bool empty = false;
+  int rc = validate(img, batch, H, W, pixel_bytes, connectivity, CCL_MODE_BINARY, labels_i32,
+                    n_regions_out, &empty);
+  if (rc != CCL_OK) return rc;
+  if (pixel_bytes < 4 && (ignore_value >> (8 * pixel_bytes)) != 0u) return CCL_ERR_INVALID_ARG;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (empty) return empty_call(batch, n_regions_out, st);
+  Layout L;
+  rc = make_layout(batch, H, W, &L);
+  if (rc != CCL_OK) return rc;
+  if (workspace) {
+    if ((uintptr_t)workspace & 255) return CCL_ERR_INVALID_ARG;
+    if (workspace_bytes < L.total) return CCL_ERR_NO_MEMORY;
+    int* status = nullptr;
+    rc = device_status_ptr(&status);
+    if (rc != CCL_OK) return rc;
+    return run_pipeline(img, batch, H, W, pixel_bytes, connectivity, CCL_MODE_BINARY, ignore_value,
+                        labels_i32, n_regions_out, L, workspace, status, true, st);
+  }
+  cudaMemPool_t pool;
+  rc = device_pool(&pool);
+  if (rc != CCL_OK) return rc;
+  void* ws = nullptr;
+  if (cudaMallocFromPoolAsync(&ws, L.total, pool, st) != cudaSuccess) {
+    cudaGetLastError();
+    return CCL_ERR_NO_MEMORY;
+  }
+  int* status = nullptr;
+  rc = device_status_ptr(&status);
+  if (rc == CCL_OK)
+    rc = run_pipeline(img, batch, H, W, pixel_bytes, connectivity, CCL_MODE_BINARY, ignore_value,
+                      labels_i32, n_regions_out, L, ws, status, true, st);
   if (cudaFreeAsync(ws, st) != cudaSuccess && rc == CCL_OK) rc = CCL_ERR_CUDA;
   return rc;
 }
@@ -527,8 +570,8 @@ extern "C" int ccl_label_noalloc(const void* img, int batch, int H, int W, int p
     cudaGetLastError();
     return CCL_ERR_CUDA;
   }
-  rc = run_pipeline(img, batch, H, W, pixel_bytes, connectivity, mode, labels_i32, n_regions_out,
-                    L, scratch + NOALLOC_STATUS_BYTES, status, false, st);
+  rc = run_pipeline(img, batch, H, W, pixel_bytes, connectivity, mode, 0u, labels_i32,
+                    n_regions_out, L, scratch + NOALLOC_STATUS_BYTES, status, false, st);
   if (rc == CCL_OK && n_regions_out) {
     k_noalloc_report<<<(batch + 255) / 256, 256, 0, st>>>(status, n_regions_out, batch);
     g_launches += 1;

@@ -31,6 +31,10 @@
 //                 leaders before it in raster order; every pixel takes its
 //                 tile-local leader's label.
 //
+// In the ignoring modes (binary: value 0; or one named value, "every-colour"
+// ch. 08 switch 4 "Ignore the paper") pixels equal to Geom::bgval are
+// background: label 0, part of no run's joins.
+//
 // Leaders are always the smallest raster index of their set (ch. 04: the
 // larger leader points at the smaller one), so the labels come out in the
 // raster order of each region's first pixel.
@@ -71,6 +75,7 @@ struct Geom {
   int wshift;
   int vec_img;                  // image rows allow 8-pixel vector loads
   int vec_out;                  // leader-map and label rows allow vector access
+  uint32_t bgval;               // background value when background is ignored
 };
 
 // Per-tile border data written by k_tile_local:
@@ -339,7 +344,7 @@ __global__ void __launch_bounds__(NT) k_tile_local(const T* __restrict__ img, ui
     if (BIN) {
 #pragma unroll
       for (int j = 0; j < PX; ++j)
-        if (c[j] == 0) fg &= ~(1u << j);
+        if (c[j] == g.bgval) fg &= ~(1u << j);
     }
     const uint32_t cl = __shfl_up_sync(FULL, c[PX - 1], 1);
     const unsigned fgl = __shfl_up_sync(FULL, fg, 1);
@@ -584,7 +589,7 @@ __global__ void __launch_bounds__(NT) k_seams(const T* __restrict__ img, const u
   // ---- top row of the tile
   if (x < t.tw) {
     const uint32_t c = cc[x + 1];
-    if (!(BIN && c == 0)) {
+    if (!(BIN && c == g.bgval)) {
       const bool hasL = t.x0 + x > 0, hasR = t.x0 + x + 1 < g.W;
       const bool eqL = hasL && cc[x] == c;
       const bool eqU = top && ca[x + 1] == c;
@@ -628,7 +633,7 @@ __global__ void __launch_bounds__(NT) k_seams(const T* __restrict__ img, const u
     const uint32_t cq = recL[2 * TH + r], cUL = recL[2 * TH + r - 1];  // (r, x0-1), (r-1, x0-1)
     const int lp = (int)recT[TH + r], lU = (int)recT[TH + r - 1];
     const int lq = (int)recL[3 * TH + r], lUL = (int)recL[3 * TH + r - 1];
-    const bool fgp = !BIN || cp != 0, fgq = !BIN || cq != 0;
+    const bool fgp = !BIN || cp != g.bgval, fgq = !BIN || cq != g.bgval;
     const bool eqL = fgp && cp == cq;
     if (eqL) join_once(lp, lq);
     if (CONN == 8) {

@@ -95,6 +95,24 @@ int ccl_label_ws(const void* img, int batch, int H, int W, int pixel_bytes,
                  size_t workspace_bytes, ccl_stream_t stream);
 
 /*
+ * ccl_label_ignore -- label every pixel except those whose pixel_bytes
+ * bytes equal `ignore_value` (little-endian; it must fit in pixel_bytes):
+ * those keep label 0 and join nothing ("every-colour", ch. 08 switch 4
+ * "Ignore the paper": if the caller names a colour to ignore, its pixels get
+ * label 0 in Start and take part in nothing after).  ignore_value 0 is the
+ * same as CCL_MODE_BINARY.  The other pixels are labelled as in
+ * CCL_MODE_ALL: 1..n by first pixel in raster order.
+ * `workspace` as in ccl_label_ws (ccl_workspace_bytes bytes, 256-byte
+ * aligned), or NULL to take scratch from the library's per-device pool.
+ * Returns CCL_ERR_INVALID_ARG if ignore_value does not fit in pixel_bytes.
+ */
+int ccl_label_ignore(const void* img, int batch, int H, int W,
+                     int pixel_bytes, int connectivity, uint32_t ignore_value,
+                     int32_t* labels_i32, int32_t* n_regions_out,
+                     void* workspace, size_t workspace_bytes,
+                     ccl_stream_t stream);
+
+/*
  * ccl_label_host -- the whole call from host memory: copies `img_host` to
  * the device, labels it and copies the labels (and counts) back into
  * `labels_host` / `n_regions_host` (host pointers; page-locked memory is

@@ -28,7 +28,8 @@ def test_header_declares_the_entry_points():
     names = declared_functions()
     for n in ("ccl_label", "ccl_label_ws", "ccl_workspace_bytes", "ccl_label_host",
               "ccl_last_status", "ccl_status_string", "ccl_set_option", "ccl_stage_times",
-              "ccl_stage_name", "ccl_kernel_launches", "ccl_label_noalloc", "ccl_version"):
+              "ccl_stage_name", "ccl_kernel_launches", "ccl_label_noalloc", "ccl_label_ignore",
+              "ccl_version"):
         assert n in names
     assert sorted(ccl.EXPORTED) == names
 
@@ -82,6 +83,18 @@ def test_invalid_arguments_rejected_on_host(lib, args, expect):
     assert ccl.ccl_label(img, B, H, W, pb, conn, mode, labels, None, None) == expect
     assert ccl.ccl_label_ws(img, B, H, W, pb, conn, mode, labels, None, FAKE * 128, 1 << 20,
                             None) == expect
+
+
+def test_ignore_value_must_fit_the_pixel(lib):
+    labels = FAKE * 64
+    assert ccl.ccl_label_ignore(FAKE, 1, 8, 8, 1, 8, 0x100, labels, None, None, 0, None) == \
+        ccl.CCL_ERR_INVALID_ARG
+    assert ccl.ccl_label_ignore(FAKE, 1, 8, 8, 2, 8, 0x10000, labels, None, None, 0, None) == \
+        ccl.CCL_ERR_INVALID_ARG
+    assert ccl.ccl_label_ignore(FAKE, 1, 8, 8, 1, 6, 0, labels, None, None, 0, None) == \
+        ccl.CCL_ERR_INVALID_ARG
+    assert ccl.ccl_label_ignore(FAKE, 1, 8, 8, 1, 8, 0, labels, None, FAKE * 128 + 8, 1 << 20,
+                                None) == ccl.CCL_ERR_INVALID_ARG
 
 
 def test_null_labels_and_overlap_rejected(lib):

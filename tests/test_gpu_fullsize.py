@@ -78,3 +78,17 @@ def test_c4_sheet_24000x33600():
     assert img.shape == (24000, 33600)
     _, n = compare(img, 8, ccl.CCL_MODE_ALL)
     assert n > 1_000_000
+
+
+def test_c4_sheet_paper_ignored():
+    # "every-colour", ch. 08 switch 4: the sheet with its white paper ignored
+    img = workloads.c4_sheet(device=DEV)
+    white = 0xFFFFFFFF
+    need = ccl.ccl_workspace_bytes(1, 24000, 33600, 4, 8, 0)
+    ws = torch.empty(need, dtype=torch.uint8, device=DEV)
+    lab, n = ccl.label_ignore(img, white, connectivity=8, workspace=ws)
+    ccl.check_status()
+    del ws
+    olab, on = oracle.label_ignore(img.cpu().numpy().view(np.uint32), white, 8)
+    assert int(n) == int(on)
+    assert np.array_equal(lab.cpu().numpy(), olab)

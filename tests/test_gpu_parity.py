@@ -200,3 +200,41 @@ def test_other_stream_and_batch_offsets():
     ccl.check_status(s)
     np.testing.assert_array_equal(lab.cpu().numpy(), olab)
     np.testing.assert_array_equal(n.cpu().numpy(), on)
+
+
+# ------------------------------------------------------ ignoring one value
+
+@pytest.mark.parametrize("shape", [(1, 1), (17, 257), (100, 1000), (255, 31)])
+@pytest.mark.parametrize("dtype", [torch.uint8, torch.int16, torch.int32])
+@pytest.mark.parametrize("conn", [4, 8])
+@pytest.mark.parametrize("ignore", [0, 2])
+def test_ignore_random_shapes(shape, dtype, conn, ignore):
+    H, W = shape
+    g = torch.Generator().manual_seed(H * 31 + W + conn + 7 * ignore)
+    img = torch.randint(0, 3, (2, H, W), generator=g).to(dtype)
+    lab, n = ccl.label_ignore(img.to(DEV), ignore, connectivity=conn)
+    ccl.check_status()
+    olab, on = oracle.label_ignore(to_np(img), ignore, conn)
+    np.testing.assert_array_equal(n.cpu().numpy(), on)
+    np.testing.assert_array_equal(lab.cpu().numpy(), olab)
+
+
+@pytest.mark.parametrize("conn", [4, 8])
+def test_ignore_paper_of_a_drawing(conn):
+    img = workloads.drawing(777, 1111, seed=5, n_segments=300, n_rects=12, levels=16,
+                            hatched=False)
+    white = 0xFFFFFFFF
+    lab, n = ccl.label_ignore(img.to(DEV), white, connectivity=conn)
+    ccl.check_status()
+    olab, on = oracle.label_ignore(to_np(img), white, conn)
+    assert int(n) == int(on)
+    np.testing.assert_array_equal(lab.cpu().numpy(), olab)
+    assert (lab.cpu().numpy()[to_np(img) == white] == 0).all()
+
+
+def test_ignore_zero_equals_binary_mode():
+    img = workloads.random_levels(333, 555, 3, seed=12).to(DEV)
+    a, na = ccl.label_ignore(img, 0, connectivity=8)
+    b, nb = ccl.label(img, 8, "binary")
+    ccl.check_status()
+    assert torch.equal(a, b) and torch.equal(na, nb)
