@@ -301,12 +301,16 @@ __device__ __forceinline__ int warp_sum(int v) {
 
 // ------------------------------------------------------------------ kernels
 
+// Occupancy matters more than a few spilled registers here: the in-tile
+// union-find is latency-bound, so the kernel is held to 32 registers (8
+// blocks of 256 threads per SM) and keeps no copy of the image in shared
+// memory (Connect re-reads the two rows it compares; a sibling warp of the
+// block has just loaded them, so they come from L1).
 template <typename T, int CONN, bool BIN>
-__global__ void __launch_bounds__(NT) k_tile_local(const T* __restrict__ img, uint16_t* __restrict__ L16,
+__global__ void __launch_bounds__(NT, 8) k_tile_local(const T* __restrict__ img, uint16_t* __restrict__ L16,
                                                    int32_t* __restrict__ P, uint32_t* __restrict__ bm,
                                                    uint32_t* __restrict__ cnt, Border bd, Geom g,
                                                    int cap, int* status) {
-  __shared__ __align__(16) T col[TILE];
   __shared__ int nborder;
   __shared__ __align__(16) int par[TILE];
   __shared__ __align__(16) uint8_t mark[TILE];
@@ -371,7 +375,6 @@ __global__ void __launch_bounds__(NT) k_tile_local(const T* __restrict__ img, ui
     int4* pp = reinterpret_cast<int4*>(par + r * TW + xl);
     pp[0] = make_int4(pv[0], pv[1], pv[2], pv[3]);
     pp[1] = make_int4(pv[4], pv[5], pv[6], pv[7]);
-    st8s<T>(col + r * TW + xl, c);
     // leader map, first pass: every pixel's run start (background LBG);
     // Collapse overwrites the entries of run starts with their leader
     uint32_t lw[PX / 2];
@@ -402,8 +405,10 @@ __global__ void __launch_bounds__(NT) k_tile_local(const T* __restrict__ img, ui
     const int r = warp + k * NWARPS;
     if (r >= t.th || r == 0) continue;   // warp-uniform
     uint32_t c[PX], u[PX];
-    ld8s<T>(col + r * TW + xl, c);
-    ld8s<T>(col + (r - 1) * TW + xl, u);
+    // this row and the row above, again from the image (a sibling warp of
+    // this block has just read them: L1 hits)
+    load8<T>(im + (long long)(t.y0 + r) * g.W + t.x0 + xl, vec, nval, c);
+    load8<T>(im + (long long)(t.y0 + r - 1) * g.W + t.x0 + xl, vec, nval, u);
     const uint32_t uL = __shfl_up_sync(FULL, u[PX - 1], 1);
     const uint32_t uR = __shfl_down_sync(FULL, u[0], 1);
     const unsigned fg = fgm[k], eq = eqm[k];
@@ -498,7 +503,7 @@ __global__ void __launch_bounds__(NT) k_tile_local(const T* __restrict__ img, ui
     const int i = r * TW + (right ? t.tw - 1 : 0);
     const int p = par[i];
     const int lead = p < 0 ? -1 : find_s(par, i, cap, status);
-    rec[2 * right * TH + r] = (uint32_t)col[i];
+    rec[2 * right * TH + r] = (uint32_t)im[(long long)(t.y0 + r) * g.W + t.x0 + (right ? t.tw - 1 : 0)];
     rec[(2 * right + 1) * TH + r] =
         lead < 0 ? 0xFFFFFFFFu : (uint32_t)((t.y0 + (lead >> LOG_TW)) * g.W + t.x0 + (lead & (TW - 1)));
   }
@@ -750,7 +755,7 @@ __device__ __forceinline__ int number_of(int gidx, const uint32_t* bmi, const ui
 // (halving on the way), takes that leader's label and stores it negated in
 // its own slot.  A walk that meets a slot already holding a negated label
 // stops there: every node on a walk belongs to the same region.
-__global__ void __launch_bounds__(NT) k_resolve(Border bd, long long nTiles, int32_t* P,
+__global__ void __launch_bounds__(NT, 8) k_resolve(Border bd, long long nTiles, int32_t* P,
                                                 const uint32_t* __restrict__ bm,
                                                 const uint32_t* __restrict__ off, Geom g, int cap,
                                                 int* status) {
@@ -795,7 +800,7 @@ __global__ void __launch_bounds__(NT) k_resolve(Border bd, long long nTiles, int
 // tile-local leader, two hops away in the leader map.  The labels buffer holds the slots of border leaders
 // until this kernel overwrites it; a tile reads only its own slots, before
 // writing.
-__global__ void __launch_bounds__(NT) k_number(const uint16_t* __restrict__ L16, int32_t* labels,
+__global__ void __launch_bounds__(NT, 8) k_number(const uint16_t* __restrict__ L16, int32_t* labels,
                                                const uint32_t* __restrict__ bm,
                                                const uint32_t* __restrict__ off, Geom g, int* status) {
   __shared__ __align__(16) int lab[TILE];
