@@ -170,38 +170,40 @@ int device_pool(cudaMemPool_t* out) {
 
 // Kernel templates are instantiated for every pixel width (1, 2, 4 bytes),
 // connectivity (4, 8) and mode (all, binary).
-#define CCL_DISPATCH(KERNEL, ...)                                                        \
+#define CCL_DISPATCH(KERNEL, GRID, BLOCK, ...)                                                        \
   do {                                                                                   \
-    const unsigned grid_ = (unsigned)L.nTiles;                                           \
+    const unsigned grid_ = (unsigned)(GRID);                                             \
+    const unsigned block_ = (unsigned)(BLOCK);                                           \
     const bool bin_ = mode == CCL_MODE_BINARY;                                           \
     if (pb == 1) {                                                                       \
-      if (conn == 8) { if (bin_) KERNEL<uint8_t, 8, true><<<grid_, NT, 0, st>>>((const uint8_t*)img, __VA_ARGS__); \
-                       else KERNEL<uint8_t, 8, false><<<grid_, NT, 0, st>>>((const uint8_t*)img, __VA_ARGS__); } \
-      else { if (bin_) KERNEL<uint8_t, 4, true><<<grid_, NT, 0, st>>>((const uint8_t*)img, __VA_ARGS__); \
-             else KERNEL<uint8_t, 4, false><<<grid_, NT, 0, st>>>((const uint8_t*)img, __VA_ARGS__); } \
+      if (conn == 8) { if (bin_) KERNEL<uint8_t, 8, true><<<grid_, block_, 0, st>>>((const uint8_t*)img, __VA_ARGS__); \
+                       else KERNEL<uint8_t, 8, false><<<grid_, block_, 0, st>>>((const uint8_t*)img, __VA_ARGS__); } \
+      else { if (bin_) KERNEL<uint8_t, 4, true><<<grid_, block_, 0, st>>>((const uint8_t*)img, __VA_ARGS__); \
+             else KERNEL<uint8_t, 4, false><<<grid_, block_, 0, st>>>((const uint8_t*)img, __VA_ARGS__); } \
     } else if (pb == 2) {                                                                \
-      if (conn == 8) { if (bin_) KERNEL<uint16_t, 8, true><<<grid_, NT, 0, st>>>((const uint16_t*)img, __VA_ARGS__); \
-                       else KERNEL<uint16_t, 8, false><<<grid_, NT, 0, st>>>((const uint16_t*)img, __VA_ARGS__); } \
-      else { if (bin_) KERNEL<uint16_t, 4, true><<<grid_, NT, 0, st>>>((const uint16_t*)img, __VA_ARGS__); \
-             else KERNEL<uint16_t, 4, false><<<grid_, NT, 0, st>>>((const uint16_t*)img, __VA_ARGS__); } \
+      if (conn == 8) { if (bin_) KERNEL<uint16_t, 8, true><<<grid_, block_, 0, st>>>((const uint16_t*)img, __VA_ARGS__); \
+                       else KERNEL<uint16_t, 8, false><<<grid_, block_, 0, st>>>((const uint16_t*)img, __VA_ARGS__); } \
+      else { if (bin_) KERNEL<uint16_t, 4, true><<<grid_, block_, 0, st>>>((const uint16_t*)img, __VA_ARGS__); \
+             else KERNEL<uint16_t, 4, false><<<grid_, block_, 0, st>>>((const uint16_t*)img, __VA_ARGS__); } \
     } else {                                                                             \
-      if (conn == 8) { if (bin_) KERNEL<uint32_t, 8, true><<<grid_, NT, 0, st>>>((const uint32_t*)img, __VA_ARGS__); \
-                       else KERNEL<uint32_t, 8, false><<<grid_, NT, 0, st>>>((const uint32_t*)img, __VA_ARGS__); } \
-      else { if (bin_) KERNEL<uint32_t, 4, true><<<grid_, NT, 0, st>>>((const uint32_t*)img, __VA_ARGS__); \
-             else KERNEL<uint32_t, 4, false><<<grid_, NT, 0, st>>>((const uint32_t*)img, __VA_ARGS__); } \
+      if (conn == 8) { if (bin_) KERNEL<uint32_t, 8, true><<<grid_, block_, 0, st>>>((const uint32_t*)img, __VA_ARGS__); \
+                       else KERNEL<uint32_t, 8, false><<<grid_, block_, 0, st>>>((const uint32_t*)img, __VA_ARGS__); } \
+      else { if (bin_) KERNEL<uint32_t, 4, true><<<grid_, block_, 0, st>>>((const uint32_t*)img, __VA_ARGS__); \
+             else KERNEL<uint32_t, 4, false><<<grid_, block_, 0, st>>>((const uint32_t*)img, __VA_ARGS__); } \
     }                                                                                    \
   } while (0)
 
 void k_tile_local_dispatch(int pb, int conn, int mode, const void* img, uint16_t* L16, int32_t* P,
                            uint32_t* bm, uint32_t* cnt, const Border& bd, const Layout& L,
                            const Geom& g, int cap, int* status, cudaStream_t st) {
-  CCL_DISPATCH(k_tile_local, L16, P, bm, cnt, bd, g, cap, status);
+  CCL_DISPATCH(k_tile_local, L.nTiles, NT, L16, P, bm, cnt, bd, g, cap, status);
 }
 
 void k_seams_dispatch(int pb, int conn, int mode, const void* img, const uint16_t* L16, int32_t* P,
                       uint32_t* bm, uint32_t* cnt, const Border& bd, const Layout& L,
                       const Geom& g, int cap, int* status, cudaStream_t st) {
-  CCL_DISPATCH(k_seams, L16, P, bm, cnt, bd, g, cap, status);
+  CCL_DISPATCH(k_seams, (L.nTiles + SEAM_WARPS - 1) / SEAM_WARPS, 32 * SEAM_WARPS, L16, P, bm, cnt, bd, g,
+               L.nTiles, cap, status);
 }
 
 // The whole labelling pipeline on `st`: `ws` is the workspace (layout L),

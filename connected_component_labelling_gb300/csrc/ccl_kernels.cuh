@@ -314,6 +314,7 @@ __global__ void __launch_bounds__(NT, 8) k_tile_local(const T* __restrict__ img,
   __shared__ int nborder;
   __shared__ __align__(16) int par[TILE];
   __shared__ __align__(16) uint8_t mark[TILE];
+  __shared__ __align__(16) uint16_t jlist[NWARPS][TW];   // a row's joins, dealt out to the lanes
   const TileCoord t = tile_coord(g);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, xl = lane * PX;
   const long long ioff = (long long)t.b * g.HW;
@@ -435,13 +436,47 @@ __global__ void __launch_bounds__(NT, 8) k_tile_local(const T* __restrict__ img,
       todo = mU & ~(eq & mUL);
     }
     const int i0 = r * TW + xl;
-    while (todo) {
-      const int bpos = __ffs(todo) - 1;
-      todo &= todo - 1;
-      const int j = bpos & 7;
-      const int d = (bpos >> 3) == 0 ? 0 : ((bpos >> 3) == 1 ? -1 : 1);
-      const int a = i0 + j, b = i0 + j - TW + d;
-      if (par[a] != par[b]) union_s(par, a, b, cap, status);   // else joined already
+    // A lane walks its own joins one after another, so a warp loops as often
+    // as its busiest lane.  When some lane has more than one join, the row's
+    // joins are first listed in shared memory (tile index | direction << 12)
+    // and dealt out to all 32 lanes.
+    const int nj = __popc(todo);
+    bool own = !__any_sync(FULL, nj > 1);
+    int total = 0, pos = 0;
+    if (!own) {
+      int inc = nj;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(FULL, inc, o);
+        if (lane >= o) inc += y;
+      }
+      total = __shfl_sync(FULL, inc, 31);
+      pos = inc - nj;
+      own = total > TW;   // more than the list holds: keep them in place
+    }
+    if (own) {
+      while (todo) {
+        const int bpos = __ffs(todo) - 1;
+        todo &= todo - 1;
+        const int j = bpos & 7;
+        const int d = (bpos >> 3) == 0 ? 0 : ((bpos >> 3) == 1 ? -1 : 1);
+        const int a = i0 + j, b = i0 + j - TW + d;
+        if (par[a] != par[b]) union_s(par, a, b, cap, status);   // else joined already
+      }
+    } else {
+      while (todo) {
+        const int bpos = __ffs(todo) - 1;
+        todo &= todo - 1;
+        jlist[warp][pos++] = (uint16_t)((i0 + (bpos & 7)) | ((bpos >> 3) << 12));
+      }
+      __syncwarp();
+      for (int q = lane; q < total; q += 32) {
+        const int e = jlist[warp][q];
+        const int a = e & (TILE - 1), dc = e >> 12;
+        const int b = a - TW + (dc == 0 ? 0 : (dc == 1 ? -1 : 1));
+        if (par[a] != par[b]) union_s(par, a, b, cap, status);
+      }
+      __syncwarp();
     }
   }
   __syncthreads();
@@ -533,120 +568,190 @@ __global__ void __launch_bounds__(NT, 8) k_tile_local(const T* __restrict__ img,
 
 // Connect across tile seams: the joins of the same rule as inside a tile,
 // evaluated on the true neighbourhood, whose partner lies in another tile.
-// A tile handles its top seam (its first row against the row above, read
-// whole and coalesced) and its left seam (its left column against the left
-// tile's right column, from the border records).
+// A tile handles its top seam (its first row against the row above) and its
+// left seam (its left column against the left tile's right column, from the
+// border records).
+//
+// One warp per tile, SEAM_WARPS tiles per block, so that many tiles' global
+// walks are in flight on an SM at once (the kernel is bound by the latency
+// of those dependent loads, not by its few bytes).  A lane owns 8
+// consecutive columns of the seam rows, as in k_tile_local.  The warp first
+// keeps every distinct pair of leaders to join once (a small hash set: along
+// a seam many joins link the same two regions), then its lanes unite the
+// kept pairs side by side.
+constexpr int SEAM_WARPS = 4;
+constexpr int SEAM_HASH = 128;
+
 template <typename T, int CONN, bool BIN>
-__global__ void __launch_bounds__(NT) k_seams(const T* __restrict__ img, const uint16_t* __restrict__ L16,
-                                              int32_t* P, uint32_t* bm, uint32_t* cnt, Border bd,
-                                              Geom g, int cap, int* status) {
-  static_assert(NT == TW, "one thread per column of the tile");
-  __shared__ uint32_t cc[TW + 2], ca[TW + 2];   // rows y0 and y0-1, columns x0-1 .. x0+TW
-  __shared__ uint16_t lc[TW], la[TW];           // leader map of the same rows
-  // pairs of leaders already joined by this tile: many joins along a seam
-  // link the same two regions, and only the first needs a global union
-  constexpr int HSIZE = 2 * NT;
+__global__ void __launch_bounds__(32 * SEAM_WARPS, 16) k_seams(const T* __restrict__ img,
+                                                               const uint16_t* __restrict__ L16, int32_t* P,
+                                                               uint32_t* bm, uint32_t* cnt, Border bd, Geom g,
+                                                               long long nTiles, int cap, int* status) {
+  __shared__ __align__(16) uint16_t lcS[SEAM_WARPS][TW], laS[SEAM_WARPS][TW];   // leader map, rows y0 and y0-1
+  __shared__ unsigned long long seenS[SEAM_WARPS][SEAM_HASH];
   constexpr unsigned long long EMPTY = ~0ull;
-  __shared__ unsigned long long seen[HSIZE];
-  for (int i = threadIdx.x; i < HSIZE; i += NT) seen[i] = EMPTY;
-  const TileCoord t = tile_coord(g);
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31, xl = lane * PX;
+  const long long tile = (long long)blockIdx.x * SEAM_WARPS + w;
+  if (tile >= nTiles) return;   // the whole warp; nothing below waits on the block
+  uint16_t* lc = lcS[w];
+  uint16_t* la = laS[w];
+  unsigned long long* seen = seenS[w];
+#pragma unroll
+  for (int i = lane; i < SEAM_HASH; i += 32) seen[i] = EMPTY;
+  const TileCoord t = tile_coord_of(g, tile);
   const long long ioff = (long long)t.b * g.HW;
   const T* im = img + ioff;
   const uint16_t* Li = L16 + ioff;
   int32_t* Pi = P + ioff;
   uint32_t* bmi = bm + (long long)t.b * g.H * g.WPR;
   uint32_t* cnti = cnt + (long long)t.b * g.H * g.CPR;
-  const int x = threadIdx.x;
   const bool top = t.y0 > 0;
   const long long row = (long long)t.y0 * g.W + t.x0;
-  if (x < t.tw) {
-    cc[x + 1] = im[row + x];
-    lc[x] = Li[row + x];
-    if (top) {
-      ca[x + 1] = im[row - g.W + x];
-      la[x] = Li[row - g.W + x];
+  const int nval = max(0, min(PX, t.tw - xl));
+  const bool vimg = g.vec_img && nval == PX;
+  const bool vmap = g.vec_out && nval == PX;
+
+  // ---- the two seam rows: colours in registers, leader-map entries in
+  // shared memory (a walk's second hop may land in another lane's columns)
+  uint32_t c[PX], u[PX];
+  load8<T>(im + row + xl, vimg, nval, c);
+  if (vmap) {
+    *reinterpret_cast<uint4*>(lc + xl) = __ldg(reinterpret_cast<const uint4*>(Li + row + xl));
+  } else {
+#pragma unroll
+    for (int j = 0; j < PX; ++j) lc[xl + j] = j < nval ? Li[row + xl + j] : LBG;
+  }
+  if (top) {
+    load8<T>(im + row - g.W + xl, vimg, nval, u);
+    if (vmap) {
+      *reinterpret_cast<uint4*>(la + xl) = __ldg(reinterpret_cast<const uint4*>(Li + row - g.W + xl));
+    } else {
+#pragma unroll
+      for (int j = 0; j < PX; ++j) la[xl + j] = j < nval ? Li[row - g.W + xl + j] : LBG;
     }
+  } else {
+#pragma unroll
+    for (int j = 0; j < PX; ++j) u[j] = 0;
   }
-  if (x == 0 && t.x0 > 0) {
-    cc[0] = im[row - 1];
-    if (top) ca[0] = im[row - g.W - 1];
+  // neighbours beyond the tile's columns: left of column 0, above-right of
+  // the last column
+  uint32_t cEdge = 0, uEdge = 0;
+  if (lane == 0 && t.x0 > 0) {
+    cEdge = im[row - 1];
+    if (top) uEdge = im[row - g.W - 1];
   }
-  if (x == 1 && t.x0 + t.tw < g.W) {
-    cc[t.tw + 1] = im[row + t.tw];
-    if (top) ca[t.tw + 1] = im[row - g.W + t.tw];
+  const bool rightTile = t.tw == TW && t.x0 + TW < g.W;
+  if (lane == 31 && rightTile && top) uEdge = im[row - g.W + TW];
+  // (every lane takes part in each shuffle; the edge lanes then substitute)
+  const uint32_t cls = __shfl_up_sync(FULL, c[PX - 1], 1);
+  const uint32_t uls = __shfl_up_sync(FULL, u[PX - 1], 1);
+  const uint32_t urs = __shfl_down_sync(FULL, u[0], 1);
+  const uint32_t cl = lane == 0 ? cEdge : cls;
+  const uint32_t ul = lane == 0 ? uEdge : uls;
+  const uint32_t ur = lane == 31 ? uEdge : urs;
+  const unsigned vmask = (1u << nval) - 1u;
+  unsigned fg = vmask;
+  if (BIN) {
+#pragma unroll
+    for (int j = 0; j < PX; ++j)
+      if (c[j] == g.bgval) fg &= ~(1u << j);
   }
-  __syncthreads();
+  const bool hasL0 = lane > 0 || t.x0 > 0;                 // column xl-1 exists
+  const bool hasR7 = nval == PX && t.x0 + xl + PX < g.W;   // column xl+8 exists
+  unsigned eqL = 0, eqU = 0, eqUL = 0, eqUR = 0;
+#pragma unroll
+  for (int j = 0; j < PX; ++j) {
+    const uint32_t cj = c[j];
+    eqL |= (j > 0 ? cj == c[j - 1] : (hasL0 && cj == cl)) ? (1u << j) : 0u;
+    eqU |= (cj == u[j]) ? (1u << j) : 0u;
+    eqUL |= (j > 0 ? cj == u[j - 1] : (hasL0 && cj == ul)) ? (1u << j) : 0u;
+    if (CONN == 8) eqUR |= (j < PX - 1 ? cj == u[j + 1] : (hasR7 && cj == ur)) ? (1u << j) : 0u;
+  }
+  eqL &= fg;
+  const unsigned upm = top ? fg : 0u;
+  eqU &= upm;
+  eqUL &= upm;
+  eqUR &= upm & ((vmask >> 1) | (hasR7 ? 0x80u : 0u));
+  unsigned todo;   // bit j: up, j+8: up-left, j+16: up-right
+  if (CONN == 8)
+    todo = (eqU & ~eqL) | ((eqUL & ~eqU & ~eqL) << 8) | ((eqUR & ~eqU) << 16);
+  else
+    todo = eqU & ~(eqL & eqUL);
+  __syncwarp();
+
   const int n = (int)g.HW;
-  auto join_once = [&](int a, int b) {
+  // keep a pair of leaders once; unite at once when the set is crowded
+  auto keep = [&](int a, int b) {
     if (a == b || a < 0 || b < 0 || a >= n || b >= n) return;
     const unsigned long long key =
         ((unsigned long long)(unsigned)min(a, b) << 32) | (unsigned)max(a, b);
-    unsigned h = (unsigned)((key * 0x9E3779B97F4A7C15ull) >> 40) & (HSIZE - 1);
+    unsigned h = (unsigned)((key * 0x9E3779B97F4A7C15ull) >> 40) & (SEAM_HASH - 1);
     for (int probe = 0; probe < 8; ++probe) {
       const unsigned long long prev = atomicCAS(&seen[h], EMPTY, key);
-      if (prev == key) return;                 // joined already by this tile
-      if (prev == EMPTY) break;                // first time: join it
-      h = (h + 1) & (HSIZE - 1);
+      if (prev == EMPTY || prev == key) return;
+      h = (h + 1) & (SEAM_HASH - 1);
     }
     union_g(Pi, a, b, bmi, cnti, g, cap, status);
   };
-
-  // ---- top row of the tile
-  if (x < t.tw) {
-    const uint32_t c = cc[x + 1];
-    if (!(BIN && c == g.bgval)) {
-      const bool hasL = t.x0 + x > 0, hasR = t.x0 + x + 1 < g.W;
-      const bool eqL = hasL && cc[x] == c;
-      const bool eqU = top && ca[x + 1] == c;
-      const bool eqUL = top && hasL && ca[x] == c;
-      const bool eqUR = (CONN == 8) && top && hasR && ca[x + 2] == c;
-      // this pixel's leader: the map gives its run start (in this row), whose
-      // entry gives the leader; a run start's own entry already is the leader
-      const int l1 = lc[x], l2 = (l1 >> LOG_TW) == 0 ? lc[l1 & (TW - 1)] : l1;
-      const int a = (t.y0 + (l2 >> LOG_TW)) * g.W + t.x0 + (l2 & (TW - 1));
-      auto up = [&](int d) {
-        const int xx = x + d;
-        int b;
-        if (xx >= 0 && xx < t.tw) {   // the tile above: its last row is row y0-1
-          const int m1 = la[xx], m2 = (m1 >> LOG_TW) == TH - 1 ? la[m1 & (TW - 1)] : m1;
-          b = (t.y0 - TH + (m2 >> LOG_TW)) * g.W + t.x0 + (m2 & (TW - 1));
-        } else {
-          b = leader_of(Li, t.y0 - 1, t.x0 + xx, g);
-        }
-        join_once(a, b);
-      };
-      if (CONN == 8) {
-        if (eqU && !eqL) up(0);
-        if (eqUL && !eqU && !eqL) up(-1);
-        if (eqUR && !eqU) up(1);
-      } else {
-        if (eqU && !(eqL && eqUL)) up(0);
-      }
-      if (eqL && x == 0) {   // left neighbour in the left tile: its border record
-        join_once(a, (int)bd.rec[((long long)blockIdx.x - 1) * 4 * TH + 3 * TH]);
-      }
+  // leader of (y0, x): the map gives the run start (in this row), whose entry
+  // gives the leader; a run start's own entry already is the leader
+  auto leader_here = [&](int x) {
+    const int l1 = lc[x], l2 = (l1 >> LOG_TW) == 0 ? lc[l1 & (TW - 1)] : l1;
+    return (t.y0 + (l2 >> LOG_TW)) * g.W + t.x0 + (l2 & (TW - 1));
+  };
+  while (todo) {
+    const int bpos = __ffs(todo) - 1;
+    todo &= todo - 1;
+    const int x = xl + (bpos & 7);
+    const int xx = x + ((bpos >> 3) == 0 ? 0 : ((bpos >> 3) == 1 ? -1 : 1));
+    int b;
+    if (xx >= 0 && xx < t.tw) {   // the tile above: its last row is row y0-1
+      const int m1 = la[xx], m2 = (m1 >> LOG_TW) == TH - 1 ? la[m1 & (TW - 1)] : m1;
+      b = (t.y0 - TH + (m2 >> LOG_TW)) * g.W + t.x0 + (m2 & (TW - 1));
+    } else {
+      b = leader_of(Li, t.y0 - 1, t.x0 + xx, g);
     }
+    keep(leader_here(x), b);
   }
+  // the first column's left neighbour lies in the left tile: its border record
+  if (lane == 0 && (eqL & 1u)) keep(leader_here(0), (int)bd.rec[(tile - 1) * 4 * TH + 3 * TH]);
 
   // ---- left column of the tile (rows below the first) against the left
   // tile's right column
-  if (t.x0 > 0 && x >= 1 && x < t.th) {
-    const int r = x;
-    const uint32_t* recT = bd.rec + (long long)blockIdx.x * 4 * TH;
+  if (t.x0 > 0 && lane >= 1 && lane < t.th) {
+    const int r = lane;
+    const uint32_t* recT = bd.rec + tile * 4 * TH;
     const uint32_t* recL = recT - 4 * TH;
     const uint32_t cp = recT[r], cU = recT[r - 1];                     // (r, x0), (r-1, x0)
     const uint32_t cq = recL[2 * TH + r], cUL = recL[2 * TH + r - 1];  // (r, x0-1), (r-1, x0-1)
     const int lp = (int)recT[TH + r], lU = (int)recT[TH + r - 1];
     const int lq = (int)recL[3 * TH + r], lUL = (int)recL[3 * TH + r - 1];
     const bool fgp = !BIN || cp != g.bgval, fgq = !BIN || cq != g.bgval;
-    const bool eqL = fgp && cp == cq;
-    if (eqL) join_once(lp, lq);
+    const bool eqLc = fgp && cp == cq;
+    if (eqLc) keep(lp, lq);
     if (CONN == 8) {
-      const bool eqU = cp == cU, eqUL = fgp && cp == cUL;
-      if (eqUL && !eqU && !eqL) join_once(lp, lUL);
+      const bool eqUc = cp == cU, eqULc = fgp && cp == cUL;
+      if (eqULc && !eqUc && !eqLc) keep(lp, lUL);
       // (r, x0-1) joins its up-right (r-1, x0) unless its own up matches
-      if (fgq && cq == cU && cq != cUL) join_once(lq, lU);
+      if (fgq && cq == cU && cq != cUL) keep(lq, lU);
     }
+  }
+  __syncwarp();
+  // ---- every kept pair, the warp's lanes side by side: the pairs are first
+  // packed to the front of the set (in place: a slot moves only to a lower
+  // or its own index, after its chunk has been read)
+  int kept = 0;
+#pragma unroll
+  for (int base = 0; base < SEAM_HASH; base += 32) {
+    const unsigned long long key = seen[base + lane];
+    const unsigned bal = __ballot_sync(FULL, key != EMPTY);
+    if (key != EMPTY) seen[kept + __popc(bal & ((1u << lane) - 1u))] = key;
+    kept += __popc(bal);
+    __syncwarp();
+  }
+  for (int i = lane; i < kept; i += 32) {
+    const unsigned long long key = seen[i];
+    union_g(Pi, (int)(key >> 32), (int)(key & 0xffffffffu), bmi, cnti, g, cap, status);
   }
 }
 
