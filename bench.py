@@ -7,7 +7,7 @@ headline target is quoted on.  One step is one ccl_label call over the whole
 sheet (all four stages: Start, Connect, Collapse, Number).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
-                    [--workload c0|c1|c2|c3:<structure>:<conn>:<mode>|c4]
+                    [--workload c0|c1|c2|c3:<structure>:<conn>:<mode>|c4|c4i|c4:HxW|flat:HxW]
 
 Prints ONE JSON line (rank 0).  Device time: CUDA events on the launching
 stream around exactly K steps, inputs resident in HBM.  Per-stage times come
@@ -59,6 +59,12 @@ def make_workload(name, device):
         H, W = (int(v) for v in name[3:].split("x"))
         img = wl.c4_sheet(device=device, H=H, W=W)
         return (dict(workload="c4_sheet_%dx%d_rgba" % (H, W), batch=1, H=H, W=W,
+                     pixel_bytes=4, connectivity=8, mode="all"), img, 4, 8, 0)
+    if name.startswith("flat:"):    # one colour everywhere, e.g. flat:6000x8400: the fixed cost
+        H, W = (int(v) for v in name[5:].split("x"))
+        import torch
+        img = torch.full((H, W), -1, dtype=torch.int32, device=device)
+        return (dict(workload="flat_%dx%d_rgba" % (H, W), batch=1, H=H, W=W,
                      pixel_bytes=4, connectivity=8, mode="all"), img, 4, 8, 0)
     if name == "c0":
         img = wl.c0_drawing(device=device)
