@@ -28,6 +28,12 @@ _LIB = os.path.join(_BUILD, "libccl_oracle.so")
 MODE_ALL = 0
 MODE_BINARY = 1
 
+# one region's statistics, the layout of the oracle's C struct (40 bytes)
+STAT_DTYPE = np.dtype([("area", np.int32), ("y_min", np.int32), ("x_min", np.int32),
+                       ("y_max", np.int32), ("x_max", np.int32), ("first", np.int32),
+                       ("sum_y", np.int64), ("sum_x", np.int64)])
+assert STAT_DTYPE.itemsize == 40
+
 _lock = threading.Lock()
 _lib = None
 
@@ -60,6 +66,10 @@ def _load():
                 ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
                 ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
                 ctypes.c_void_p, ctypes.c_void_p]
+            lib.oracle_region_stats.restype = ctypes.c_int
+            lib.oracle_region_stats.argtypes = [
+                ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64]
             _lib = lib
     return _lib
 
@@ -125,3 +135,23 @@ def label(img: np.ndarray, connectivity: int = 8, mode: int = MODE_ALL):
     if squeeze:
         return labels[0], n[0]
     return labels, n
+
+
+def region_stats(labels: np.ndarray, n_regions):
+    """Statistics of every labelled region (see ``oracle_region_stats`` in
+    ``ccl_oracle.c`` for the definitions and citations): a structured array
+    of ``STAT_DTYPE`` with one entry per region, image by image, label 1 first.
+    ``labels`` is [B,]H,W int32, ``n_regions`` the region count per image."""
+    lab = np.ascontiguousarray(labels, dtype=np.int32)
+    if lab.ndim == 2:
+        lab = lab[None]
+    B, H, W = lab.shape
+    n = np.ascontiguousarray(np.asarray(n_regions, dtype=np.int32).reshape(-1))
+    if n.shape[0] != B:
+        raise ValueError("one region count per image")
+    total = int(n.astype(np.int64).sum())
+    out = np.empty(max(total, 1), dtype=STAT_DTYPE)
+    rc = _load().oracle_region_stats(lab.ctypes.data, B, H, W, n.ctypes.data, out.ctypes.data, total)
+    if rc != 0:
+        raise RuntimeError("oracle_region_stats failed with status %d" % rc)
+    return out[:total]

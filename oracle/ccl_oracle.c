@@ -161,3 +161,77 @@ static int label_all(const void* img, int64_t batch, int64_t H, int64_t W,
   free(queue);
   return ORACLE_OK;
 }
+
+/*
+ * Region statistics: the step that usually follows labelling.  The lpnh.cn
+ * page (CUDA image segmentation, §1.1) labels the regions so that their
+ * area and position can be measured next; "GPU Connected Component Labeling"
+ * (mcclanahoochie.com, closing section) names statistics on every labelled
+ * region as the next image-processing step; bendabir.com (Prologue) uses the
+ * labels to cut out each area's bounding box.  The pages define no formula
+ * beyond the names, so the plain definitions are taken:
+ *
+ *   area         number of pixels carrying the label;
+ *   y_min .. x_max  the smallest and largest row and column among them
+ *                (inclusive bounding box);
+ *   first        raster index y*W + x, inside the image, of the first of them
+ *                in reading order;
+ *   sum_y, sum_x sums of their row and column indices (the centroid is
+ *                sum / area).
+ *
+ * Layout (40 bytes): six int32 (area, y_min, x_min, y_max, x_max, first),
+ * then two int64 (sum_y, sum_x).  The entry of label l (1..n_regions[b]) of
+ * image b is at index n_regions[0] + ... + n_regions[b-1] + l - 1.  A label
+ * that no pixel carries keeps area 0, box (INT32_MAX, INT32_MAX, -1, -1),
+ * first INT32_MAX and zero sums.  Labels must lie in 0..n_regions[b]
+ * (0 = background, counted nowhere); any other value gives
+ * ORACLE_ERR_INVALID_ARG.  Host pointers only.
+ */
+typedef struct {
+  int32_t area, y_min, x_min, y_max, x_max, first;
+  int64_t sum_y, sum_x;
+} oracle_region_stat;
+
+int oracle_region_stats(const int32_t* labels, int64_t batch, int64_t H,
+                        int64_t W, const int32_t* n_regions,
+                        oracle_region_stat* out, int64_t capacity) {
+  if (batch < 0 || H < 0 || W < 0 || capacity < 0) return ORACLE_ERR_INVALID_ARG;
+  int64_t total = 0;
+  for (int64_t b = 0; b < batch; ++b) {
+    if (n_regions[b] < 0) return ORACLE_ERR_INVALID_ARG;
+    total += n_regions[b];
+  }
+  if (total > capacity) return ORACLE_ERR_NO_MEMORY;
+  for (int64_t e = 0; e < total; ++e) {
+    out[e].area = 0;
+    out[e].y_min = INT32_MAX;
+    out[e].x_min = INT32_MAX;
+    out[e].y_max = -1;
+    out[e].x_max = -1;
+    out[e].first = INT32_MAX;
+    out[e].sum_y = 0;
+    out[e].sum_x = 0;
+  }
+  int64_t base = 0;
+  for (int64_t b = 0; b < batch; ++b) {
+    const int32_t* lab = labels + b * H * W;
+    for (int64_t y = 0; y < H; ++y) {
+      for (int64_t x = 0; x < W; ++x) {
+        const int32_t l = lab[y * W + x];
+        if (l == 0) continue;
+        if (l < 0 || l > n_regions[b]) return ORACLE_ERR_INVALID_ARG;
+        oracle_region_stat* s = &out[base + l - 1];
+        if (s->area == 0) s->first = (int32_t)(y * W + x);   /* reading order */
+        s->area += 1;
+        if (y < s->y_min) s->y_min = (int32_t)y;
+        if (x < s->x_min) s->x_min = (int32_t)x;
+        if (y > s->y_max) s->y_max = (int32_t)y;
+        if (x > s->x_max) s->x_max = (int32_t)x;
+        s->sum_y += y;
+        s->sum_x += x;
+      }
+    }
+    base += n_regions[b];
+  }
+  return ORACLE_OK;
+}
