@@ -32,7 +32,12 @@ CCL_OPT_STAGE_EVENTS = 2
 EXPORTED = ("ccl_label", "ccl_workspace_bytes", "ccl_label_ws", "ccl_label_host",
             "ccl_last_status", "ccl_status_string", "ccl_set_option", "ccl_stage_times",
             "ccl_stage_name", "ccl_kernel_launches", "ccl_label_noalloc", "ccl_label_ignore",
-            "ccl_version")
+            "ccl_region_stats_workspace_bytes", "ccl_region_stats", "ccl_version")
+
+# one region's statistics (struct ccl_region_stat, 40 bytes): six int32 then two int64
+STAT_BYTES = 40
+STAT_FIELDS_I32 = ("area", "y_min", "x_min", "y_max", "x_max", "first")
+STAT_FIELDS_I64 = ("sum_y", "sum_x")
 
 _lock = threading.Lock()
 _lib = None
@@ -79,6 +84,10 @@ def lib():
             L.ccl_label_ignore.argtypes = [vp, i32, i32, i32, i32, i32, ctypes.c_uint32, vp, vp,
                                            vp, sz, vp]
             L.ccl_label_ignore.restype = i32
+            L.ccl_region_stats_workspace_bytes.argtypes = [i32]
+            L.ccl_region_stats_workspace_bytes.restype = sz
+            L.ccl_region_stats.argtypes = [vp, i32, i32, i32, vp, vp, ctypes.c_int64, vp, sz, vp]
+            L.ccl_region_stats.restype = i32
             L.ccl_version.argtypes = []
             L.ccl_version.restype = i32
             _lib = L
@@ -182,6 +191,53 @@ def label_ignore(img, ignore_value, connectivity=8, out=None, n_out=None, worksp
     if squeeze:
         return out.view(H, W), n_out.view(())
     return out, n_out
+
+
+def ccl_region_stats_workspace_bytes(batch):
+    return lib().ccl_region_stats_workspace_bytes(batch)
+
+
+def ccl_region_stats(labels, batch, H, W, n_regions, stats, capacity, workspace, workspace_bytes,
+                     stream):
+    return lib().ccl_region_stats(labels, batch, H, W, n_regions, stats, capacity, workspace,
+                                  workspace_bytes, stream)
+
+
+def region_stats(labels, n_regions, capacity=None, workspace=None, stream=None):
+    """Statistics of every region of a label tensor from ``label`` /
+    ``label_ignore`` (``n_regions``: their region counts, on the device).
+    Returns ``(raw, fields)``: ``raw`` the uint8 tensor of ``capacity``
+    40-byte entries (image by image, label 1 first), ``fields`` a dict of
+    views into it -- int32 ``area``, ``y_min``, ``x_min``, ``y_max``,
+    ``x_max``, ``first`` and int64 ``sum_y``, ``sum_x``.  ``capacity``
+    defaults to the total number of regions (read from the device, which
+    synchronises).  Device-side findings are reported by ``check_status``."""
+    import torch
+    if not labels.is_cuda:
+        raise ValueError("region_stats() needs CUDA tensors; the library has no CPU path")
+    labels = labels.contiguous()
+    if labels.dim() == 2:
+        B, (H, W) = 1, labels.shape
+    else:
+        B, H, W = labels.shape
+    n = n_regions.reshape(-1).to(torch.int32).contiguous()
+    if capacity is None:
+        capacity = int(n.to(torch.int64).sum().item())
+    raw = torch.empty((max(capacity, 1) * STAT_BYTES,), dtype=torch.uint8, device=labels.device)
+    st = stream if stream is not None else torch.cuda.current_stream(labels.device)
+    wp, wb = (workspace.data_ptr(), workspace.numel() * workspace.element_size()) \
+        if workspace is not None else (None, 0)
+    with torch.cuda.device(labels.device):
+        rc = ccl_region_stats(labels.data_ptr(), B, H, W, n.data_ptr(), raw.data_ptr(), capacity,
+                              wp, wb, st.cuda_stream)
+    if rc != CCL_OK:
+        raise CCLError(rc, "ccl_region_stats")
+    raw = raw[:capacity * STAT_BYTES]
+    i32 = raw.view(torch.int32).view(capacity, STAT_BYTES // 4)
+    i64 = raw.view(torch.int64).view(capacity, STAT_BYTES // 8)
+    fields = {f: i32[:, k] for k, f in enumerate(STAT_FIELDS_I32)}
+    fields.update({f: i64[:, 3 + k] for k, f in enumerate(STAT_FIELDS_I64)})
+    return raw, fields
 
 
 def ccl_version():

@@ -495,7 +495,63 @@ int ccl_last_status(ccl_stream_t stream) {
   int h = 0;
   if (cudaMemcpy(&h, status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return CCL_ERR_CUDA;
   if (h != 0 && cudaMemset(status, 0, sizeof(int)) != cudaSuccess) return CCL_ERR_CUDA;
-  return h != 0 ? CCL_ERR_DEVICE_LIMIT : CCL_OK;
+  if (h & (FLAG_WALK_CAP | FLAG_INTERNAL)) return CCL_ERR_DEVICE_LIMIT;
+  if (h & FLAG_STATS_CAP) return CCL_ERR_NO_MEMORY;
+  if (h & FLAG_BAD_LABEL) return CCL_ERR_INVALID_ARG;
+  return CCL_OK;
+}
+
+size_t ccl_region_stats_workspace_bytes(int batch) {
+  if (batch < 0) return 0;
+  return align_up((size_t)(batch + 1) * sizeof(long long), 256);
+}
+
+int ccl_region_stats(const int32_t* labels_i32, int batch, int H, int W, const int32_t* n_regions,
+                     ccl_region_stat* stats, int64_t capacity, void* workspace,
+                     size_t workspace_bytes, ccl_stream_t stream) {
+  if (batch < 0 || H < 0 || W < 0 || capacity < 0) return CCL_ERR_INVALID_ARG;
+  if ((long long)H * W >= (1ll << 31)) return CCL_ERR_TOO_LARGE;
+  if (batch == 0 || H == 0 || W == 0) return CCL_OK;
+  if (!labels_i32 || !n_regions || ((uintptr_t)labels_i32 & 3) || ((uintptr_t)n_regions & 3))
+    return CCL_ERR_INVALID_ARG;
+  if (capacity > 0 && (!stats || ((uintptr_t)stats & 7))) return CCL_ERR_INVALID_ARG;
+  const size_t need = ccl_region_stats_workspace_bytes(batch);
+  if (workspace) {
+    if ((uintptr_t)workspace & 255) return CCL_ERR_INVALID_ARG;
+    if (workspace_bytes < need) return CCL_ERR_NO_MEMORY;
+  }
+  Layout L;
+  int rc = make_layout(batch, H, W, &L);
+  if (rc != CCL_OK) return rc;
+  Geom g = L.g;
+  g.vec_out = (W % 8 == 0) && ((uintptr_t)labels_i32 % 16 == 0);
+  int* status = nullptr;
+  rc = device_status_ptr(&status);
+  if (rc != CCL_OK) return rc;
+  cudaStream_t st = (cudaStream_t)stream;
+  void* ws = workspace;
+  cudaMemPool_t pool = nullptr;
+  if (!ws) {
+    rc = device_pool(&pool);
+    if (rc != CCL_OK) return rc;
+    if (cudaMallocFromPoolAsync(&ws, need, pool, st) != cudaSuccess) {
+      cudaGetLastError();
+      return CCL_ERR_NO_MEMORY;
+    }
+  }
+  long long* off = (long long*)ws;
+  k_stats_offsets<<<1, NT, 0, st>>>(n_regions, batch, off, status);
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    sms = 1;
+  k_stats_init<<<(unsigned)(sms * 8), NT, 0, st>>>(stats, (long long)capacity, off, batch, status);
+  k_region_stats<<<(unsigned)L.nTiles, NT, 0, st>>>(labels_i32, n_regions, off, stats,
+                                                   (long long)capacity, g, status);
+  g_launches += 3;
+  rc = cudaPeekAtLastError() == cudaSuccess ? CCL_OK : CCL_ERR_CUDA;
+  if (!workspace && cudaFreeAsync(ws, st) != cudaSuccess && rc == CCL_OK) rc = CCL_ERR_CUDA;
+  return rc;
 }
 
 }  // extern "C"

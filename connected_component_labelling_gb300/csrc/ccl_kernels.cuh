@@ -31,6 +31,10 @@
 //                 leaders before it in raster order; every pixel takes its
 //                 tile-local leader's label.
 //
+// After labelling, on request (ccl_region_stats): region statistics --
+// area, bounding box, first pixel, coordinate sums -- as a reduction over the
+// final labels: k_stats_offsets, k_stats_init, k_region_stats.
+//
 // In the ignoring modes (binary: value 0; or one named value, "every-colour"
 // ch. 08 switch 4 "Ignore the paper") pixels equal to Geom::bgval are
 // background: label 0, part of no run's joins.
@@ -41,7 +45,10 @@
 #pragma once
 
 #include <cuda_runtime.h>
+#include <limits.h>
 #include <stdint.h>
+
+#include "ccl.h"
 
 namespace ccl_dev {
 
@@ -63,6 +70,8 @@ static_assert(TH % NWARPS == 0, "whole rows per warp");
 
 constexpr int FLAG_WALK_CAP = 1;    // a union-find walk or retry loop hit its cap
 constexpr int FLAG_INTERNAL = 2;    // an invariant of the numbering pass failed
+constexpr int FLAG_STATS_CAP = 4;   // more regions than the statistics array holds
+constexpr int FLAG_BAD_LABEL = 8;   // a label outside 0..n of its image, or a negative count
 
 struct Geom {
   int H, W;
@@ -994,6 +1003,200 @@ __global__ void __launch_bounds__(NT, 8) k_number(const uint16_t* __restrict__ L
       for (int j = 0; j < PX; ++j)
         if (j < nval) orow[j] = out[j];
     }
+  }
+}
+
+// ------------------------------------------------------ region statistics
+// The step after labelling on the pages: regions are labelled so that their
+// area and position can be measured (CUDA image segmentation, lpnh.cn,
+// §1.1), statistics on every labelled region come next ("GPU Connected
+// Component Labeling", mcclanahoochie.com, closing section), and each area
+// gets its bounding box (bendabir.com, Prologue).  A reduction by label, as
+// the lpnh.cn page builds its global reductions (§2.3, §6.1): each block
+// first sums into a private table in shared memory, and only the block's
+// totals go to global memory with atomics.
+
+// per-image offsets of the statistics entries: off[b] = n[0] + ... + n[b-1],
+// off[batch] = the total (one block)
+__global__ void __launch_bounds__(NT) k_stats_offsets(const int32_t* __restrict__ n, int batch,
+                                                      long long* off, int* status) {
+  __shared__ long long wsum[NWARPS];
+  __shared__ long long carry;
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  if (threadIdx.x == 0) carry = 0;
+  __syncthreads();
+  for (int base = 0; base < batch; base += NT) {
+    const int i = base + threadIdx.x;
+    long long v = i < batch ? (long long)n[i] : 0;
+    if (v < 0) {
+      raise_flag(status, FLAG_BAD_LABEL);
+      v = 0;
+    }
+    long long inc = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const long long y = __shfl_up_sync(FULL, inc, o);
+      if (lane >= o) inc += y;
+    }
+    if (lane == 31) wsum[wid] = inc;
+    __syncthreads();
+    long long before = carry, total = 0;
+#pragma unroll
+    for (int w = 0; w < NWARPS; ++w) {
+      if (w < wid) before += wsum[w];
+      total += wsum[w];
+    }
+    if (i < batch) off[i] = before + inc - v;
+    __syncthreads();
+    if (threadIdx.x == 0) carry += total;
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) off[batch] = carry;
+}
+
+// every entry below min(total, capacity): the empty statistics
+__global__ void k_stats_init(ccl_region_stat* stats, long long capacity, const long long* off,
+                             int batch, int* status) {
+  const long long total = off[batch];
+  const long long n = total < capacity ? total : capacity;
+  if (blockIdx.x == 0 && threadIdx.x == 0 && total > capacity) raise_flag(status, FLAG_STATS_CAP);
+  for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < n;
+       e += (long long)gridDim.x * blockDim.x) {
+    ccl_region_stat z;
+    z.area = 0;
+    z.y_min = INT_MAX;
+    z.x_min = INT_MAX;
+    z.y_max = -1;
+    z.x_max = -1;
+    z.first = INT_MAX;
+    z.sum_y = 0;
+    z.sum_x = 0;
+    stats[e] = z;
+  }
+}
+
+// one segment's contribution to one entry of the global array
+__device__ __forceinline__ void stats_add_global(ccl_region_stat* e, int area, int y_min, int x_min,
+                                                 int y_max, int x_max, int first,
+                                                 unsigned long long sy, unsigned long long sx) {
+  atomicAdd(&e->area, area);
+  atomicMin(&e->y_min, y_min);
+  atomicMin(&e->x_min, x_min);
+  atomicMax(&e->y_max, y_max);
+  atomicMax(&e->x_max, x_max);
+  atomicMin(&e->first, first);
+  atomicAdd(reinterpret_cast<unsigned long long*>(&e->sum_y), sy);
+  atomicAdd(reinterpret_cast<unsigned long long*>(&e->sum_x), sx);
+}
+
+// A block per 256 x 16 tile, a lane per 8 consecutive labels of a row (as
+// in k_tile_local).  A lane splits its 8 labels into runs of equal label;
+// each run adds its length, row, end columns, first raster index and
+// coordinate sums to the tile's table (open addressing on the label); a run
+// whose label finds no free slot goes straight to the global entry.  Then
+// every table entry is added to its global entry.
+constexpr int STATS_HASH = 512;
+
+__global__ void __launch_bounds__(NT) k_region_stats(const int32_t* __restrict__ labels,
+                                                     const int32_t* __restrict__ n_regions,
+                                                     const long long* __restrict__ off,
+                                                     ccl_region_stat* stats, long long capacity,
+                                                     Geom g, int* status) {
+  __shared__ int hkey[STATS_HASH], harea[STATS_HASH], hymin[STATS_HASH], hxmin[STATS_HASH];
+  __shared__ int hymax[STATS_HASH], hxmax[STATS_HASH], hfirst[STATS_HASH];
+  __shared__ unsigned long long hsy[STATS_HASH], hsx[STATS_HASH];
+  for (int i = threadIdx.x; i < STATS_HASH; i += NT) {
+    hkey[i] = 0;   // labels start at 1
+    harea[i] = 0;
+    hymin[i] = INT_MAX;
+    hxmin[i] = INT_MAX;
+    hymax[i] = -1;
+    hxmax[i] = -1;
+    hfirst[i] = INT_MAX;
+    hsy[i] = 0;
+    hsx[i] = 0;
+  }
+  __syncthreads();
+  const TileCoord t = tile_coord(g);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, xl = lane * PX;
+  const int nb = n_regions[t.b];
+  const long long base = off[t.b];
+  const int32_t* li = labels + (long long)t.b * g.HW;
+  const int nval = max(0, min(PX, t.tw - xl));
+  const bool vec = g.vec_out && nval == PX;
+  const unsigned vmask = (1u << nval) - 1u;
+  auto add = [&](int l, int y, int xs, int xe) {
+    const int len = xe - xs + 1;
+    const int first = y * g.W + xs;
+    const unsigned long long sy = (unsigned long long)y * (unsigned long long)len;
+    const unsigned long long sx = (unsigned long long)(xs + xe) * (unsigned long long)len / 2ull;
+    unsigned h = ((unsigned)l * 2654435761u) >> 23;   // 9 bits: STATS_HASH slots
+    for (int probe = 0; probe < 8; ++probe) {
+      const int prev = atomicCAS(&hkey[h], 0, l);
+      if (prev == 0 || prev == l) {
+        atomicAdd(&harea[h], len);
+        atomicMin(&hymin[h], y);
+        atomicMin(&hxmin[h], xs);
+        atomicMax(&hymax[h], y);
+        atomicMax(&hxmax[h], xe);
+        atomicMin(&hfirst[h], first);
+        atomicAdd(&hsy[h], sy);
+        atomicAdd(&hsx[h], sx);
+        return;
+      }
+      h = (h + 1) & (STATS_HASH - 1);
+    }
+    const long long e = base + l - 1;   // the table is crowded: straight to the global entry
+    if (e < capacity) stats_add_global(stats + e, len, y, xs, y, xe, first, sy, sx);
+  };
+#pragma unroll
+  for (int k = 0; k < RPW; ++k) {
+    const int r = warp + k * NWARPS;
+    if (r >= t.th) continue;
+    const int y = t.y0 + r;
+    const int32_t* row = li + (long long)y * g.W + t.x0 + xl;
+    int v[PX];
+    if (vec) {
+      const int4 a = __ldg(reinterpret_cast<const int4*>(row));
+      const int4 b = __ldg(reinterpret_cast<const int4*>(row) + 1);
+      v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+      v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+    } else {
+#pragma unroll
+      for (int j = 0; j < PX; ++j) v[j] = j < nval ? __ldg(row + j) : 0;
+    }
+    // runs of equal label inside the lane: starts and ends
+    unsigned same = 0;   // bit j: v[j] == v[j-1]
+#pragma unroll
+    for (int j = 1; j < PX; ++j) same |= (v[j] == v[j - 1] ? 1u : 0u) << j;
+    const unsigned starts = vmask & ~same;
+    // an end: the next label differs, or the pixel is the lane's last valid one
+    const unsigned ends = vmask & (~(same >> 1) | (vmask ^ (vmask >> 1)));
+    unsigned m = ends;
+    while (m) {
+      const int e = __ffs(m) - 1;
+      m &= m - 1;
+      const int s = 31 - __clz(starts & ((2u << e) - 1u));
+      int l = v[0];
+#pragma unroll
+      for (int j = 1; j < PX; ++j)
+        if (j == e) l = v[j];
+      if (l == 0) continue;
+      if (l < 0 || l > nb) {
+        raise_flag(status, FLAG_BAD_LABEL);
+        continue;
+      }
+      add(l, y, t.x0 + xl + s, t.x0 + xl + e);
+    }
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < STATS_HASH; i += NT) {
+    const int l = hkey[i];
+    if (l == 0) continue;
+    const long long e = base + l - 1;
+    if (e < capacity)
+      stats_add_global(stats + e, harea[i], hymin[i], hxmin[i], hymax[i], hxmax[i], hfirst[i], hsy[i],
+                       hsx[i]);
   }
 }
 

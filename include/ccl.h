@@ -129,9 +129,10 @@ int ccl_label_host(const void* img_host, int batch, int H, int W,
  * ccl_last_status -- synchronises `stream`, then returns and clears the
  * current device's sticky device-side status: CCL_ERR_DEVICE_LIMIT if a
  * bounded loop (a union-find walk or a union retry) reached its cap in any
- * call since the last check, CCL_ERR_CUDA if the stream reports an error,
- * else CCL_OK.  The caps are far above any legitimate walk; tripping one
- * means the labels of that call are not valid.
+ * call since the last check, CCL_ERR_NO_MEMORY / CCL_ERR_INVALID_ARG for the
+ * device-side findings of ccl_region_stats (see there), CCL_ERR_CUDA if the
+ * stream reports an error, else CCL_OK.  The caps are far above any
+ * legitimate walk; tripping one means the labels of that call are not valid.
  */
 int ccl_last_status(ccl_stream_t stream);
 
@@ -199,6 +200,56 @@ int ccl_label_noalloc(const void* img, int batch, int H, int W,
                       int pixel_bytes, int connectivity, int mode,
                       int32_t* labels_i32, int32_t* n_regions_out,
                       ccl_stream_t stream);
+
+/*
+ * Region statistics, the step after labelling: regions are labelled so that
+ * their area and position can be measured (CUDA image segmentation, lpnh.cn,
+ * §1.1); statistics on every labelled region are the next image-processing
+ * step ("GPU Connected Component Labeling", mcclanahoochie.com, closing
+ * section); each area's bounding box (bendabir.com, Prologue).  Per region:
+ *   area            number of pixels carrying the label;
+ *   y_min .. x_max  inclusive bounding box (rows, columns);
+ *   first           raster index y*W + x, inside its image, of the region's
+ *                   first pixel in reading order (its leader);
+ *   sum_y, sum_x    sums of the rows and of the columns of its pixels (the
+ *                   centroid is sum / area).
+ * A label that no pixel carries keeps area 0, box (INT32_MAX, INT32_MAX,
+ * -1, -1), first INT32_MAX and zero sums.
+ */
+typedef struct ccl_region_stat {
+  int32_t area, y_min, x_min, y_max, x_max, first;
+  int64_t sum_y, sum_x;
+} ccl_region_stat; /* 40 bytes */
+
+/*
+ * ccl_region_stats_workspace_bytes -- scratch bytes ccl_region_stats needs
+ * for `batch` images ((batch + 1) int64 offsets, rounded up to 256); 0 for
+ * batch < 0.
+ */
+size_t ccl_region_stats_workspace_bytes(int batch);
+
+/*
+ * ccl_region_stats -- statistics of every region of `labels_i32` (device,
+ * [batch][H][W] int32, as written by ccl_label / ccl_label_ws /
+ * ccl_label_ignore: 0 is background and counted nowhere, 1..n_regions[b] in
+ * image b).  `n_regions` (device, int32[batch]) holds the region counts of
+ * the same call.  `stats` (device, 8-byte aligned, room for `capacity`
+ * entries): the entry of label l of image b is at index
+ * n_regions[0] + ... + n_regions[b-1] + l - 1, and every entry below that
+ * total is written.  `workspace`: ccl_region_stats_workspace_bytes(batch)
+ * bytes, 256-byte aligned, or NULL to take it from the library's pool.  All
+ * buffers are the caller's; the call only reads labels_i32 and n_regions.
+ * Asynchronous on `stream`.  Host-side errors are returned (bad pointer,
+ * alignment or size: CCL_ERR_INVALID_ARG; H*W >= 2^31: CCL_ERR_TOO_LARGE;
+ * workspace too small: CCL_ERR_NO_MEMORY).  Device-side findings go to
+ * ccl_last_status: CCL_ERR_NO_MEMORY if the regions outnumber `capacity`
+ * (entries at and beyond it are skipped), CCL_ERR_INVALID_ARG if a label lies
+ * outside 0..n_regions of its image or a count is negative (skipped).
+ */
+int ccl_region_stats(const int32_t* labels_i32, int batch, int H, int W,
+                     const int32_t* n_regions, ccl_region_stat* stats,
+                     int64_t capacity, void* workspace, size_t workspace_bytes,
+                     ccl_stream_t stream);
 
 /* Library version, as major*10000 + minor*100 + patch. */
 int ccl_version(void);

@@ -131,3 +131,26 @@ def test_no_cpu_path():
     import torch
     with pytest.raises(ValueError):
         ccl.label(torch.zeros((4, 4), dtype=torch.uint8))
+
+
+def test_region_stats_host_checks(lib):
+    assert ccl.ccl_region_stats_workspace_bytes(-1) == 0
+    assert ccl.ccl_region_stats_workspace_bytes(0) == 256
+    assert ccl.ccl_region_stats_workspace_bytes(31) == 256
+    assert ccl.ccl_region_stats_workspace_bytes(100) == 1024      # 101 int64 offsets
+    lab, n, st, ws = FAKE * 64, FAKE * 96, FAKE * 128, FAKE * 160
+    # empty calls touch nothing
+    assert ccl.ccl_region_stats(lab, 0, 8, 8, n, st, 10, None, 0, None) == ccl.CCL_OK
+    assert ccl.ccl_region_stats(lab, 2, 0, 8, n, st, 10, None, 0, None) == ccl.CCL_OK
+    # bad sizes, pointers and alignment are refused on the host
+    assert ccl.ccl_region_stats(lab, -1, 8, 8, n, st, 10, None, 0, None) == ccl.CCL_ERR_INVALID_ARG
+    assert ccl.ccl_region_stats(lab, 1, 8, 8, n, st, -1, None, 0, None) == ccl.CCL_ERR_INVALID_ARG
+    assert ccl.ccl_region_stats(None, 1, 8, 8, n, st, 10, None, 0, None) == ccl.CCL_ERR_INVALID_ARG
+    assert ccl.ccl_region_stats(lab, 1, 8, 8, None, st, 10, None, 0, None) == ccl.CCL_ERR_INVALID_ARG
+    assert ccl.ccl_region_stats(lab + 2, 1, 8, 8, n, st, 10, None, 0, None) == ccl.CCL_ERR_INVALID_ARG
+    assert ccl.ccl_region_stats(lab, 1, 8, 8, n, st + 4, 10, None, 0, None) == ccl.CCL_ERR_INVALID_ARG
+    assert ccl.ccl_region_stats(lab, 1, 8, 8, n, None, 10, None, 0, None) == ccl.CCL_ERR_INVALID_ARG
+    assert ccl.ccl_region_stats(lab, 1, 1 << 16, 1 << 15, n, st, 10, None, 0, None) == \
+        ccl.CCL_ERR_TOO_LARGE
+    assert ccl.ccl_region_stats(lab, 1, 8, 8, n, st, 10, ws + 16, 256, None) == ccl.CCL_ERR_INVALID_ARG
+    assert ccl.ccl_region_stats(lab, 100, 8, 8, n, st, 10, ws, 512, None) == ccl.CCL_ERR_NO_MEMORY
