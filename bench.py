@@ -271,6 +271,8 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-stats", action="store_true",
+                    help="skip timing ccl_region_stats on the labels")
     ap.add_argument("--ref-rows", type=int, default=REF_ROWS,
                     help="rows of the sheet one reference (oracle) step labels")
     args = ap.parse_args()
@@ -395,6 +397,48 @@ def main():
                      "peak": peak, "unit": "GB/s", "frac": path_gbs / peak,
                      "note": "whole ccl_label call: image read once + int32 label write"}
 
+    # ---- region statistics of the labels just made (the step after
+    # labelling), timed on their own: labels read once, one 40-byte entry
+    # written per region
+    region_stats = None
+    if not args.no_stats:
+        total = int(nreg.to(torch.int64).sum().item())
+        sraw = torch.empty(max(total, 1) * ccl.STAT_BYTES, dtype=torch.uint8, device=dev)
+        swb = ccl.ccl_region_stats_workspace_bytes(B)
+        sws = torch.empty(swb, dtype=torch.uint8, device=dev)
+
+        def sstep():
+            rc = ccl.ccl_region_stats(labels.data_ptr(), B, H, W, nreg.data_ptr(), sraw.data_ptr(),
+                                      total, sws.data_ptr(), swb, sp)
+            if rc != ccl.CCL_OK:
+                raise ccl.CCLError(rc, "ccl_region_stats")
+
+        for _ in range(3):
+            sstep()
+        ccl.check_status(stream)
+        ksteps = max(3, min(args.steps, 20))
+        sev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(ksteps)]
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        for a, b in sev:
+            if flush is not None:
+                flush.fill_(1)
+            a.record(stream)
+            sstep()
+            b.record(stream)
+        torch.cuda.synchronize(dev)
+        ccl.check_status(stream)
+        sms = max_over_ranks(sum(a.elapsed_time(b) for a, b in sev) / ksteps, world)
+        salg = 4 * px + ccl.STAT_BYTES * total
+        sgbs = salg / (sms * 1e-3) / 1e9
+        region_stats = {"api": "ccl_region_stats", "ms": sms, "value": world * px / (sms * 1e-3) / 1e9,
+                        "unit": UNIT, "steps": ksteps, "regions": total, "alg_bytes": salg,
+                        "achieved_gbs": sgbs, "peak": peak, "frac": sgbs / peak,
+                        "note": "labels read once (4 B/px) + one 40-byte entry per region; "
+                                "3 kernel launches per call"}
+        del sraw, sws
+
     # ---- e2e through the host entry point
     e2e = None
     if not args.no_e2e and mode >= 0:
@@ -449,6 +493,7 @@ def main():
                                parallelism="replicas" if world > 1 else "single"),
                 "roofline": roofline, "roofline_path": roofline_path, "stages": stages,
                 "cpu_baseline": cpu_baseline, "e2e": e2e, "gpu_launches": launches,
+                "region_stats": region_stats,
                 "clocks": clocks, "n_regions": n_regions[:8],
                 "kernel_source_sha": source_sha()}
         print(json.dumps(line), flush=True)

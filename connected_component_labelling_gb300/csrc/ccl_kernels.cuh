@@ -1089,114 +1089,171 @@ __device__ __forceinline__ void stats_add_global(ccl_region_stat* e, int area, i
   atomicAdd(reinterpret_cast<unsigned long long*>(&e->sum_x), sx);
 }
 
-// A block per 256 x 16 tile, a lane per 8 consecutive labels of a row (as
-// in k_tile_local).  A lane splits its 8 labels into runs of equal label;
-// each run adds its length, row, end columns, first raster index and
-// coordinate sums to the tile's table (open addressing on the label); a run
-// whose label finds no free slot goes straight to the global entry.  Then
-// every table entry is added to its global entry.
-constexpr int STATS_HASH = 512;
+// A block per 256-column x SR-row area; a warp per row at a time, a lane per
+// 8 consecutive labels (as in k_tile_local).  Each lane splits its labels
+// into runs of equal label; the warp's runs of one label are merged first
+// (lanes grouped by label, their lengths, ends and sums reduced across the
+// group) so that a label updates the area's table once per row.  The table
+// (open addressing on the label) keeps, per label, the area, box, first
+// pixel, coordinate sums and whether any of its pixels lies on an inner edge
+// of the area (a row or column with neighbours outside it).  A label that
+// does not is wholly inside the area -- a region that reaches outside crosses
+// that edge -- so its entry is stored outright; the others are added to the
+// global entry with atomics.  A run whose label finds no free slot goes
+// straight to the global entry.  Every label must be one 4- or 8-connected
+// set, as the labels of this library are.
+#ifndef CCL_STATS_HASH
+#define CCL_STATS_HASH 1024
+#define CCL_STATS_ROWS 16
+#define CCL_STATS_NT 256
+#endif
+constexpr int STATS_HASH = CCL_STATS_HASH;
+constexpr int SR = CCL_STATS_ROWS;       // rows of a statistics area
+constexpr int STATS_NT = CCL_STATS_NT;   // threads of a statistics block
+constexpr int STATS_NWARPS = STATS_NT / 32;
+constexpr int STATS_HASH_BITS = STATS_HASH == 4096 ? 12 : STATS_HASH == 2048 ? 11 : STATS_HASH == 1024 ? 10 : 9;
+static_assert((1 << STATS_HASH_BITS) == STATS_HASH, "a power of two");
+constexpr int EDGE_BIT = 1 << 30;   // in a table entry's area word: a pixel on an inner edge
 
-__global__ void __launch_bounds__(NT) k_region_stats(const int32_t* __restrict__ labels,
+__global__ void __launch_bounds__(STATS_NT) k_region_stats(const int32_t* __restrict__ labels,
                                                      const int32_t* __restrict__ n_regions,
                                                      const long long* __restrict__ off,
                                                      ccl_region_stat* stats, long long capacity,
                                                      Geom g, int* status) {
-  __shared__ int hkey[STATS_HASH], harea[STATS_HASH], hymin[STATS_HASH], hxmin[STATS_HASH];
-  __shared__ int hymax[STATS_HASH], hxmax[STATS_HASH], hfirst[STATS_HASH];
-  __shared__ unsigned long long hsy[STATS_HASH], hsx[STATS_HASH];
-  for (int i = threadIdx.x; i < STATS_HASH; i += NT) {
+  // per slot: label, area (+ EDGE_BIT), smallest / largest column, largest
+  // row, first raster index, and the row and column sums relative to the
+  // area's corner (the smallest row is the first pixel's)
+  __shared__ int hkey[STATS_HASH], harea[STATS_HASH], hxmin[STATS_HASH], hxmax[STATS_HASH];
+  __shared__ int hymax[STATS_HASH], hfirst[STATS_HASH];
+  __shared__ unsigned hsy[STATS_HASH], hsx[STATS_HASH];
+  for (int i = threadIdx.x; i < STATS_HASH; i += STATS_NT) {
     hkey[i] = 0;   // labels start at 1
     harea[i] = 0;
-    hymin[i] = INT_MAX;
     hxmin[i] = INT_MAX;
-    hymax[i] = -1;
     hxmax[i] = -1;
+    hymax[i] = -1;
     hfirst[i] = INT_MAX;
     hsy[i] = 0;
     hsx[i] = 0;
   }
   __syncthreads();
-  const TileCoord t = tile_coord(g);
+  // block -> image, area row, area column
+  const int areasY = (g.H + SR - 1) / SR;
+  const long long perImage = (long long)areasY * g.tilesX;
+  const int b = (int)(blockIdx.x / perImage);
+  const int rest = (int)(blockIdx.x - (long long)b * perImage);
+  const int ay = rest / g.tilesX, ax = rest - ay * g.tilesX;
+  const int y0 = ay * SR, y1 = min(y0 + SR, g.H) - 1;   // rows y0..y1
+  const int x0 = ax * TW, x1 = min(x0 + TW, g.W) - 1;   // columns x0..x1
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, xl = lane * PX;
-  const int nb = n_regions[t.b];
-  const long long base = off[t.b];
-  const int32_t* li = labels + (long long)t.b * g.HW;
-  const int nval = max(0, min(PX, t.tw - xl));
+  const int nb = n_regions[b];
+  const long long base = off[b];
+  const int32_t* li = labels + (long long)b * g.HW;
+  const int nval = max(0, min(PX, x1 - x0 + 1 - xl));
   const bool vec = g.vec_out && nval == PX;
   const unsigned vmask = (1u << nval) - 1u;
-  auto add = [&](int l, int y, int xs, int xe) {
-    const int len = xe - xs + 1;
-    const int first = y * g.W + xs;
-    const unsigned long long sy = (unsigned long long)y * (unsigned long long)len;
-    const unsigned long long sx = (unsigned long long)(xs + xe) * (unsigned long long)len / 2ull;
-    unsigned h = ((unsigned)l * 2654435761u) >> 23;   // 9 bits: STATS_HASH slots
-    for (int probe = 0; probe < 8; ++probe) {
-      const int prev = atomicCAS(&hkey[h], 0, l);
-      if (prev == 0 || prev == l) {
-        atomicAdd(&harea[h], len);
-        atomicMin(&hymin[h], y);
-        atomicMin(&hxmin[h], xs);
-        atomicMax(&hymax[h], y);
-        atomicMax(&hxmax[h], xe);
-        atomicMin(&hfirst[h], first);
-        atomicAdd(&hsy[h], sy);
-        atomicAdd(&hsx[h], sx);
-        return;
-      }
-      h = (h + 1) & (STATS_HASH - 1);
-    }
-    const long long e = base + l - 1;   // the table is crowded: straight to the global entry
-    if (e < capacity) stats_add_global(stats + e, len, y, xs, y, xe, first, sy, sx);
-  };
-#pragma unroll
-  for (int k = 0; k < RPW; ++k) {
-    const int r = warp + k * NWARPS;
-    if (r >= t.th) continue;
-    const int y = t.y0 + r;
-    const int32_t* row = li + (long long)y * g.W + t.x0 + xl;
+  // inner edges: a pixel there has neighbours outside the area
+  const bool edgeL = x0 > 0, edgeR = x1 < g.W - 1;
+  for (int y = y0 + warp; y <= y1; y += STATS_NWARPS) {
+    const int32_t* row = li + (long long)y * g.W + x0 + xl;
     int v[PX];
     if (vec) {
-      const int4 a = __ldg(reinterpret_cast<const int4*>(row));
-      const int4 b = __ldg(reinterpret_cast<const int4*>(row) + 1);
-      v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-      v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+      const int4 p = __ldg(reinterpret_cast<const int4*>(row));
+      const int4 q = __ldg(reinterpret_cast<const int4*>(row) + 1);
+      v[0] = p.x; v[1] = p.y; v[2] = p.z; v[3] = p.w;
+      v[4] = q.x; v[5] = q.y; v[6] = q.z; v[7] = q.w;
     } else {
 #pragma unroll
       for (int j = 0; j < PX; ++j) v[j] = j < nval ? __ldg(row + j) : 0;
     }
-    // runs of equal label inside the lane: starts and ends
+    const bool edgeRow = (y == y0 && y0 > 0) || (y == y1 && y1 < g.H - 1);
+    // runs of equal label inside the lane
     unsigned same = 0;   // bit j: v[j] == v[j-1]
 #pragma unroll
     for (int j = 1; j < PX; ++j) same |= (v[j] == v[j - 1] ? 1u : 0u) << j;
     const unsigned starts = vmask & ~same;
     // an end: the next label differs, or the pixel is the lane's last valid one
-    const unsigned ends = vmask & (~(same >> 1) | (vmask ^ (vmask >> 1)));
-    unsigned m = ends;
-    while (m) {
-      const int e = __ffs(m) - 1;
-      m &= m - 1;
-      const int s = 31 - __clz(starts & ((2u << e) - 1u));
-      int l = v[0];
+    unsigned ends = vmask & (~(same >> 1) | (vmask ^ (vmask >> 1)));
+    const int rounds = (int)__reduce_max_sync(FULL, (unsigned)__popc(ends));
+    for (int it = 0; it < rounds; ++it) {
+      int l = 0, s = 0, e = 0;
+      if (ends) {
+        e = __ffs(ends) - 1;
+        ends &= ends - 1;
+        s = 31 - __clz(starts & ((2u << e) - 1u));
 #pragma unroll
-      for (int j = 1; j < PX; ++j)
-        if (j == e) l = v[j];
-      if (l == 0) continue;
-      if (l < 0 || l > nb) {
-        raise_flag(status, FLAG_BAD_LABEL);
-        continue;
+        for (int j = 0; j < PX; ++j)
+          if (j == e) l = v[j];
+        if (l < 0 || l > nb) {
+          raise_flag(status, FLAG_BAD_LABEL);
+          l = 0;
+        }
       }
-      add(l, y, t.x0 + xl + s, t.x0 + xl + e);
+      // lanes holding a run of the same label this round form a group; the
+      // group's lengths, ends and column sums are combined across it
+      const unsigned grp = __match_any_sync(FULL, l);
+      const unsigned xs = (unsigned)(xl + s), xe = (unsigned)(xl + e);   // columns in the area
+      const unsigned len = l > 0 ? xe - xs + 1u : 0u;
+      const unsigned area = __reduce_add_sync(grp, len);
+      const unsigned sxs = __reduce_add_sync(grp, l > 0 ? (xs + xe) * len / 2u : 0u);
+      const unsigned xmin = __reduce_min_sync(grp, l > 0 ? xs : 0xFFFFFFFFu);
+      const unsigned xmax = __reduce_max_sync(grp, l > 0 ? xe : 0u);
+      const unsigned edge = __reduce_or_sync(
+          grp, (l > 0 && (edgeRow || (s + xl == 0 && edgeL) || (x0 + (int)xe == x1 && edgeR))) ? 1u : 0u);
+      if (l <= 0 || lane != __ffs(grp) - 1) continue;
+      // the group's first lane updates the table once
+      const int first = y * g.W + x0 + (int)xmin;
+      unsigned h = ((unsigned)l * 2654435761u) >> (32 - STATS_HASH_BITS);
+      bool kept = false;
+      for (int probe = 0; probe < 16 && !kept; ++probe) {
+        const int prev = atomicCAS(&hkey[h], 0, l);
+        if (prev == 0 || prev == l) {
+          atomicAdd(&harea[h], (int)area);
+          if (edge) atomicOr(&harea[h], EDGE_BIT);
+          atomicMin(&hxmin[h], (int)xmin);
+          atomicMax(&hxmax[h], (int)xmax);
+          atomicMax(&hymax[h], y);
+          atomicMin(&hfirst[h], first);
+          atomicAdd(&hsy[h], (unsigned)(y - y0) * area);
+          atomicAdd(&hsx[h], sxs);
+          kept = true;
+        }
+        h = (h + 1) & (STATS_HASH - 1);
+      }
+      if (!kept) {   // the table is crowded: straight to the global entry
+        const long long ge = base + l - 1;
+        if (ge < capacity)
+          stats_add_global(stats + ge, (int)area, y, x0 + (int)xmin, y, x0 + (int)xmax, first,
+                           (unsigned long long)y * area,
+                           (unsigned long long)sxs + (unsigned long long)x0 * area);
+      }
     }
   }
   __syncthreads();
-  for (int i = threadIdx.x; i < STATS_HASH; i += NT) {
+  for (int i = threadIdx.x; i < STATS_HASH; i += STATS_NT) {
     const int l = hkey[i];
     if (l == 0) continue;
-    const long long e = base + l - 1;
-    if (e < capacity)
-      stats_add_global(stats + e, harea[i], hymin[i], hxmin[i], hymax[i], hxmax[i], hfirst[i], hsy[i],
-                       hsx[i]);
+    const long long ge = base + l - 1;
+    if (ge >= capacity) continue;
+    const int area = harea[i] & (EDGE_BIT - 1);
+    const int first = hfirst[i];
+    const int ymin = div_w(first, g);
+    const unsigned long long sy = (unsigned long long)hsy[i] + (unsigned long long)y0 * area;
+    const unsigned long long sx = (unsigned long long)hsx[i] + (unsigned long long)x0 * area;
+    if (harea[i] & EDGE_BIT) {
+      stats_add_global(stats + ge, area, ymin, x0 + hxmin[i], hymax[i], x0 + hxmax[i], first, sy, sx);
+    } else {   // wholly inside this area: this block is the entry's only writer
+      ccl_region_stat r;
+      r.area = area;
+      r.y_min = ymin;
+      r.x_min = x0 + hxmin[i];
+      r.y_max = hymax[i];
+      r.x_max = x0 + hxmax[i];
+      r.first = first;
+      r.sum_y = (int64_t)sy;
+      r.sum_x = (int64_t)sx;
+      stats[ge] = r;
+    }
   }
 }
 
