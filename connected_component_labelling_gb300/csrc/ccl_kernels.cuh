@@ -1174,35 +1174,66 @@ __global__ void __launch_bounds__(STATS_NT) k_region_stats(const int32_t* __rest
     const unsigned starts = vmask & ~same;
     // an end: the next label differs, or the pixel is the lane's last valid one
     unsigned ends = vmask & (~(same >> 1) | (vmask ^ (vmask >> 1)));
-    const int rounds = (int)__reduce_max_sync(FULL, (unsigned)__popc(ends));
-    for (int it = 0; it < rounds; ++it) {
-      int l = 0, s = 0, e = 0;
-      if (ends) {
-        e = __ffs(ends) - 1;
-        ends &= ends - 1;
-        s = 31 - __clz(starts & ((2u << e) - 1u));
+    // A run that crosses from lane L into lanes L+1.. is counted once, by
+    // lane L: a segmented suffix sum over the lanes gathers the pieces of
+    // the lanes it continues into (each lane's first run, while the lanes
+    // it passes through hold nothing else).
+    const int lastv = nval > 0 ? v[nval - 1] : 0;
+    const int prevLast = __shfl_up_sync(FULL, lastv, 1);
+    const bool contL = lane > 0 && nval > 0 && v[0] == prevLast;   // my first run began to my left
+    const bool single = __popc(ends) == 1;
+    const int e0 = ends ? __ffs(ends) - 1 : 0;                      // end of my first run
+    const bool contNext = __shfl_down_sync(FULL, contL ? 1 : 0, 1) != 0 && lane < 31;
+    // the piece I hand to the lane on my left, and whether the chain goes on past me
+    unsigned pl = contL ? (unsigned)(e0 + 1) : 0u;                   // length
+    unsigned px = contL ? (unsigned)(2 * xl + e0) * (unsigned)(e0 + 1) / 2u : 0u;   // column sum
+    unsigned pm = contL ? (unsigned)(xl + e0) : 0u;                  // last column
+    unsigned pe = (contL && ((xl + e0 == x1 - x0 && edgeR) || edgeRow)) ? 1u : 0u;
+    bool brk = !(single && contNext);
 #pragma unroll
-        for (int j = 0; j < PX; ++j)
-          if (j == e) l = v[j];
-        if (l < 0 || l > nb) {
-          raise_flag(status, FLAG_BAD_LABEL);
-          l = 0;
-        }
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned nl = __shfl_down_sync(FULL, pl, o), nx = __shfl_down_sync(FULL, px, o);
+      const unsigned nm = __shfl_down_sync(FULL, pm, o), ne = __shfl_down_sync(FULL, pe, o);
+      const bool nb2 = __shfl_down_sync(FULL, brk ? 1 : 0, o) != 0;
+      if (!brk && lane + o < 32) {
+        pl += nl;
+        px += nx;
+        pm = max(pm, nm);
+        pe |= ne;
+        brk = nb2;
       }
-      // lanes holding a run of the same label this round form a group; the
-      // group's lengths, ends and column sums are combined across it
-      const unsigned grp = __match_any_sync(FULL, l);
-      const unsigned xs = (unsigned)(xl + s), xe = (unsigned)(xl + e);   // columns in the area
-      const unsigned len = l > 0 ? xe - xs + 1u : 0u;
-      const unsigned area = __reduce_add_sync(grp, len);
-      const unsigned sxs = __reduce_add_sync(grp, l > 0 ? (xs + xe) * len / 2u : 0u);
-      const unsigned xmin = __reduce_min_sync(grp, l > 0 ? xs : 0xFFFFFFFFu);
-      const unsigned xmax = __reduce_max_sync(grp, l > 0 ? xe : 0u);
-      const unsigned edge = __reduce_or_sync(
-          grp, (l > 0 && (edgeRow || (s + xl == 0 && edgeL) || (x0 + (int)xe == x1 && edgeR))) ? 1u : 0u);
-      if (l <= 0 || lane != __ffs(grp) - 1) continue;
-      // the group's first lane updates the table once
-      const int first = y * g.W + x0 + (int)xmin;
+    }
+    // the chain that continues my last run: the sums from lane + 1
+    const unsigned cl = __shfl_down_sync(FULL, pl, 1), cx = __shfl_down_sync(FULL, px, 1);
+    const unsigned cm = __shfl_down_sync(FULL, pm, 1), ce = __shfl_down_sync(FULL, pe, 1);
+    bool firstRun = true;
+    while (ends) {
+      const int e = __ffs(ends) - 1;
+      ends &= ends - 1;
+      const bool isFirst = firstRun;
+      firstRun = false;
+      if (isFirst && contL) continue;   // counted by the lane where the run began
+      const int sj = 31 - __clz(starts & ((2u << e) - 1u));
+      int l = 0;
+#pragma unroll
+      for (int j = 0; j < PX; ++j)
+        if (j == e) l = v[j];
+      if (l == 0) continue;
+      if (l < 0 || l > nb) {
+        raise_flag(status, FLAG_BAD_LABEL);
+        continue;
+      }
+      unsigned xs = (unsigned)(xl + sj), xe = (unsigned)(xl + e);   // columns in the area
+      unsigned area = xe - xs + 1u;
+      unsigned sxs = (xs + xe) * area / 2u;
+      unsigned edge = (edgeRow || (xs == 0u && edgeL) || (x0 + (int)xe == x1 && edgeR)) ? 1u : 0u;
+      if (ends == 0u && contNext) {   // my last run goes on into the next lanes
+        area += cl;
+        sxs += cx;
+        xe = max(xe, cm);
+        edge |= ce;
+      }
+      const int first = y * g.W + x0 + (int)xs;
       unsigned h = ((unsigned)l * 2654435761u) >> (32 - STATS_HASH_BITS);
       bool kept = false;
       for (int probe = 0; probe < 16 && !kept; ++probe) {
@@ -1210,8 +1241,8 @@ __global__ void __launch_bounds__(STATS_NT) k_region_stats(const int32_t* __rest
         if (prev == 0 || prev == l) {
           atomicAdd(&harea[h], (int)area);
           if (edge) atomicOr(&harea[h], EDGE_BIT);
-          atomicMin(&hxmin[h], (int)xmin);
-          atomicMax(&hxmax[h], (int)xmax);
+          atomicMin(&hxmin[h], (int)xs);
+          atomicMax(&hxmax[h], (int)xe);
           atomicMax(&hymax[h], y);
           atomicMin(&hfirst[h], first);
           atomicAdd(&hsy[h], (unsigned)(y - y0) * area);
@@ -1223,7 +1254,7 @@ __global__ void __launch_bounds__(STATS_NT) k_region_stats(const int32_t* __rest
       if (!kept) {   // the table is crowded: straight to the global entry
         const long long ge = base + l - 1;
         if (ge < capacity)
-          stats_add_global(stats + ge, (int)area, y, x0 + (int)xmin, y, x0 + (int)xmax, first,
+          stats_add_global(stats + ge, (int)area, y, x0 + (int)xs, y, x0 + (int)xe, first,
                            (unsigned long long)y * area,
                            (unsigned long long)sxs + (unsigned long long)x0 * area);
       }
