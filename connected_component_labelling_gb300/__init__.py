@@ -252,9 +252,10 @@ _MODES = {"all": CCL_MODE_ALL, "binary": CCL_MODE_BINARY,
 
 def image_geometry(img):
     """(batch, H, W, pixel_bytes, squeeze) of a [B,]H,W tensor of 1/2/4-byte
-    pixels, or a [B,]H,W,C uint8 tensor whose C bytes form one pixel."""
+    pixels, or a [B,]H,W,C uint8 tensor whose C (2, 3 or 4) bytes form one
+    pixel (C = 3: packed 24-bit RGB)."""
     import torch
-    if img.dtype == torch.uint8 and img.dim() == 4 and img.shape[-1] in (2, 4):
+    if img.dtype == torch.uint8 and img.dim() == 4 and img.shape[-1] in (2, 3, 4):
         B, H, W, pb = img.shape
         return B, H, W, pb, False
     pb = img.element_size()

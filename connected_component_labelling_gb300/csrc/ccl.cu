@@ -116,7 +116,7 @@ int validate(const void* img, int batch, int H, int W, int pb, int conn, int mod
              const int32_t* labels, const int32_t* n_out, bool* empty) {
   *empty = false;
   if (batch < 0 || H < 0 || W < 0) return CCL_ERR_INVALID_ARG;
-  if (pb != 1 && pb != 2 && pb != 4) return CCL_ERR_INVALID_ARG;
+  if (pb < 1 || pb > 4) return CCL_ERR_INVALID_ARG;
   if (conn != 4 && conn != 8) return CCL_ERR_INVALID_ARG;
   if (mode != CCL_MODE_ALL && mode != CCL_MODE_BINARY) return CCL_ERR_INVALID_ARG;
   if ((long long)H * W >= (1ll << 31)) return CCL_ERR_TOO_LARGE;
@@ -126,7 +126,8 @@ int validate(const void* img, int batch, int H, int W, int pb, int conn, int mod
     return CCL_OK;
   }
   if (!img || !labels) return CCL_ERR_INVALID_ARG;
-  if (((uintptr_t)img % (uintptr_t)pb) || ((uintptr_t)labels & 3)) return CCL_ERR_INVALID_ARG;
+  // pixels align to their size; 3-byte RGB pixels need no alignment
+  if ((pb != 3 && (uintptr_t)img % (uintptr_t)pb) || ((uintptr_t)labels & 3)) return CCL_ERR_INVALID_ARG;
   const uintptr_t n = (uintptr_t)batch * (uintptr_t)H * (uintptr_t)W;
   const uintptr_t ia = (uintptr_t)img, ib = ia + n * (uintptr_t)pb;
   const uintptr_t la = (uintptr_t)labels, lb = la + n * 4;
@@ -168,7 +169,7 @@ int device_pool(cudaMemPool_t* out) {
   return CCL_OK;
 }
 
-// Kernel templates are instantiated for every pixel width (1, 2, 4 bytes),
+// Kernel templates are instantiated for every pixel width (1, 2, 3, 4 bytes),
 // connectivity (4, 8) and mode (all, binary).
 #define CCL_DISPATCH(KERNEL, GRID, BLOCK, ...)                                                        \
   do {                                                                                   \
@@ -180,6 +181,11 @@ int device_pool(cudaMemPool_t* out) {
                        else KERNEL<uint8_t, 8, false><<<grid_, block_, 0, st>>>((const uint8_t*)img, __VA_ARGS__); } \
       else { if (bin_) KERNEL<uint8_t, 4, true><<<grid_, block_, 0, st>>>((const uint8_t*)img, __VA_ARGS__); \
              else KERNEL<uint8_t, 4, false><<<grid_, block_, 0, st>>>((const uint8_t*)img, __VA_ARGS__); } \
+    } else if (pb == 3) {                                                                \
+      if (conn == 8) { if (bin_) KERNEL<Rgb24, 8, true><<<grid_, block_, 0, st>>>((const Rgb24*)img, __VA_ARGS__); \
+                       else KERNEL<Rgb24, 8, false><<<grid_, block_, 0, st>>>((const Rgb24*)img, __VA_ARGS__); } \
+      else { if (bin_) KERNEL<Rgb24, 4, true><<<grid_, block_, 0, st>>>((const Rgb24*)img, __VA_ARGS__); \
+             else KERNEL<Rgb24, 4, false><<<grid_, block_, 0, st>>>((const Rgb24*)img, __VA_ARGS__); } \
     } else if (pb == 2) {                                                                \
       if (conn == 8) { if (bin_) KERNEL<uint16_t, 8, true><<<grid_, block_, 0, st>>>((const uint16_t*)img, __VA_ARGS__); \
                        else KERNEL<uint16_t, 8, false><<<grid_, block_, 0, st>>>((const uint16_t*)img, __VA_ARGS__); } \
@@ -240,6 +246,7 @@ int run_pipeline(const void* img, int batch, int H, int W, int pb, int conn, int
   const uintptr_t ia = (uintptr_t)img;
   if (pb == 1) g.vec_img = (W % 8 == 0) && (ia % 8 == 0);
   else if (pb == 2) g.vec_img = (W % 8 == 0) && (ia % 16 == 0);
+  else if (pb == 3) g.vec_img = (W % 8 == 0) && (ia % 8 == 0);   // 24-byte lanes on 8-byte boundaries
   else g.vec_img = (W % 4 == 0) && (ia % 16 == 0);
   g.vec_out = (W % 8 == 0) && ((uintptr_t)labels % 16 == 0);
   const unsigned grid = (unsigned)L.nTiles;
@@ -345,7 +352,7 @@ int ccl_stage_times(double* ms_sum, int max_stages, int* n_calls) {
 
 size_t ccl_workspace_bytes(int batch, int H, int W, int pixel_bytes, int connectivity, int mode) {
   if (batch <= 0 || H <= 0 || W <= 0) return 0;
-  if (pixel_bytes != 1 && pixel_bytes != 2 && pixel_bytes != 4) return 0;
+  if (pixel_bytes < 1 || pixel_bytes > 4) return 0;
   if (connectivity != 4 && connectivity != 8) return 0;
   if (mode != CCL_MODE_ALL && mode != CCL_MODE_BINARY) return 0;
   if ((long long)H * W >= (1ll << 31)) return 0;

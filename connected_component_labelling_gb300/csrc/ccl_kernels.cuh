@@ -162,6 +162,39 @@ __device__ __forceinline__ void load8<uint16_t>(const uint16_t* p, bool vec, int
   }
 }
 
+// 24-bit RGB, three bytes a pixel with no padding: the form "every-colour"
+// reads its drawings in (ch. 08 "Tried and dropped": a packed 32-bit copy of
+// the picture was slower and took twice the memory).  A pixel compares as
+// its 24-bit value.
+struct Rgb24 {
+  uint8_t v[3];
+  __device__ __forceinline__ operator uint32_t() const {
+    return (uint32_t)v[0] | ((uint32_t)v[1] << 8) | ((uint32_t)v[2] << 16);
+  }
+};
+static_assert(sizeof(Rgb24) == 3, "three bytes a pixel");
+
+// Eight RGB pixels are 24 bytes: from an 8-byte boundary, three 8-byte
+// loads (a warp reads 768 contiguous bytes) and the bytes regrouped.
+template <>
+__device__ __forceinline__ void load8<Rgb24>(const Rgb24* p, bool vec, int n, uint32_t c[PX]) {
+  if (vec) {
+    const uint2* q = reinterpret_cast<const uint2*>(p);
+    const uint2 a = __ldg(q), b = __ldg(q + 1), d = __ldg(q + 2);
+    c[0] = a.x & 0xFFFFFFu;
+    c[1] = __byte_perm(a.x, a.y, 0x0543) & 0xFFFFFFu;
+    c[2] = __byte_perm(a.y, b.x, 0x0432) & 0xFFFFFFu;
+    c[3] = b.x >> 8;
+    c[4] = b.y & 0xFFFFFFu;
+    c[5] = __byte_perm(b.y, d.x, 0x0543) & 0xFFFFFFu;
+    c[6] = __byte_perm(d.x, d.y, 0x0432) & 0xFFFFFFu;
+    c[7] = d.y >> 8;
+  } else {
+#pragma unroll
+    for (int j = 0; j < PX; ++j) c[j] = j < n ? (uint32_t)p[j] : 0u;
+  }
+}
+
 template <>
 __device__ __forceinline__ void load8<uint32_t>(const uint32_t* p, bool vec, int n, uint32_t c[PX]) {
   if (vec) {

@@ -21,8 +21,12 @@
  * Conventions for every entry point:
  *  - Images are contiguous and row-major: pixel (b, y, x) sits at byte
  *    ((b*H + y)*W + x) * pixel_bytes of `img`; labels likewise at element
- *    (b*H + y)*W + x of `labels_i32`.  `img` must be aligned to pixel_bytes,
- *    `labels_i32` and `n_regions_out` to 4 bytes.
+ *    (b*H + y)*W + x of `labels_i32`.  `img` must be aligned to pixel_bytes
+ *    (3-byte pixels: no alignment), `labels_i32` and `n_regions_out` to 4
+ *    bytes.
+ *  - pixel_bytes 3 is packed 24-bit RGB, three bytes a pixel: the form
+ *    "every-colour" reads its drawings in (ch. 08 "Tried and dropped": a
+ *    packed 32-bit copy of the picture was slower and twice the memory).
  *  - Pixel equality compares all pixel_bytes bytes (RGBA: alpha included).
  *  - Labels are canonical per image: numbering restarts at 1 in every image.
  *  - H*W must be below 2^31 (CCL_ERR_TOO_LARGE otherwise); batch*H*W may
@@ -63,7 +67,7 @@ enum { CCL_MODE_ALL = 0, CCL_MODE_BINARY = 1 };
 
 /*
  * ccl_label -- label `batch` images of H x W pixels.
- *   img            device pointer, batch*H*W pixels of pixel_bytes (1, 2 or 4)
+ *   img            device pointer, batch*H*W pixels of pixel_bytes (1, 2, 3 or 4)
  *   connectivity   4 or 8
  *   mode           CCL_MODE_ALL (every pixel labelled) or CCL_MODE_BINARY
  *                  (all-zero pixels are background, label 0)

@@ -52,7 +52,8 @@ def test_status_strings_and_version(lib):
 
 def test_workspace_bytes(lib):
     assert ccl.ccl_workspace_bytes(0, 10, 10, 1, 8, 0) == 0
-    assert ccl.ccl_workspace_bytes(1, 10, 10, 3, 8, 0) == 0       # bad pixel_bytes
+    assert ccl.ccl_workspace_bytes(1, 10, 10, 5, 8, 0) == 0       # bad pixel_bytes
+    assert ccl.ccl_workspace_bytes(1, 10, 10, 3, 8, 0) > 0        # 24-bit RGB
     assert ccl.ccl_workspace_bytes(1, 10, 10, 1, 6, 0) == 0       # bad connectivity
     assert ccl.ccl_workspace_bytes(1, 1 << 16, 1 << 15, 1, 8, 0) == 0   # H*W = 2^31
     a = ccl.ccl_workspace_bytes(1, 1024, 1024, 4, 8, 0)
@@ -68,7 +69,8 @@ FAKE = 1 << 20   # a host address never dereferenced: validation fails first
 
 
 @pytest.mark.parametrize("args,expect", [
-    ((FAKE, 1, 8, 8, 3, 8, 0), ccl.CCL_ERR_INVALID_ARG),     # pixel_bytes
+    ((FAKE, 1, 8, 8, 5, 8, 0), ccl.CCL_ERR_INVALID_ARG),     # pixel_bytes
+    ((FAKE, 1, 8, 8, 0, 8, 0), ccl.CCL_ERR_INVALID_ARG),     # pixel_bytes
     ((FAKE, 1, 8, 8, 1, 6, 0), ccl.CCL_ERR_INVALID_ARG),     # connectivity
     ((FAKE, 1, 8, 8, 1, 8, 2), ccl.CCL_ERR_INVALID_ARG),     # mode
     ((FAKE, -1, 8, 8, 1, 8, 0), ccl.CCL_ERR_INVALID_ARG),    # batch
@@ -90,6 +92,8 @@ def test_ignore_value_must_fit_the_pixel(lib):
     assert ccl.ccl_label_ignore(FAKE, 1, 8, 8, 1, 8, 0x100, labels, None, None, 0, None) == \
         ccl.CCL_ERR_INVALID_ARG
     assert ccl.ccl_label_ignore(FAKE, 1, 8, 8, 2, 8, 0x10000, labels, None, None, 0, None) == \
+        ccl.CCL_ERR_INVALID_ARG
+    assert ccl.ccl_label_ignore(FAKE, 1, 8, 8, 3, 8, 0x1000000, labels, None, None, 0, None) == \
         ccl.CCL_ERR_INVALID_ARG
     assert ccl.ccl_label_ignore(FAKE, 1, 8, 8, 1, 6, 0, labels, None, None, 0, None) == \
         ccl.CCL_ERR_INVALID_ARG

@@ -341,3 +341,11 @@ CONFIGS = {
     "c3_structures_8192": (None, None, 1),      # every structure x {4,8} x {all,binary}
     "c4_sheet_24000x33600_rgba": (8, MODE_ALL, 4),
 }
+
+
+def c4_sheet_rgb(device="cpu", H=C4_H, W=C4_W):
+    """The construction sheet as packed 24-bit RGB, uint8 [1, H, W, 3] (2.4 GB
+    at full size): the RGBA sheet without its alpha byte, which is 255
+    everywhere, so its regions are the RGBA sheet's."""
+    rgba = c4_sheet(device=device, H=H, W=W)
+    return rgba.view(torch.uint8).reshape(H, W, 4)[:, :, :3].contiguous().reshape(1, H, W, 3)
