@@ -7,7 +7,7 @@ headline target is quoted on.  One step is one ccl_label call over the whole
 sheet (all four stages: Start, Connect, Collapse, Number).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
-                    [--workload c0|c1|c2|c3:<structure>:<conn>:<mode>|c4|c4i|c4:HxW|flat:HxW]
+                    [--workload c0|c1|c2|c3:<structure>:<conn>:<mode>|c4|c4i|c4rgb|c4:HxW|flat:HxW]
 
 Prints ONE JSON line (rank 0).  Device time: CUDA events on the launching
 stream around exactly K steps, inputs resident in HBM.  Per-stage times come
@@ -55,6 +55,10 @@ def make_workload(name, device):
         return (dict(workload="c4_sheet_24000x33600_rgba_paper_ignored", batch=1, H=wl.C4_H,
                      W=wl.C4_W, pixel_bytes=4, connectivity=8, mode="ignore",
                      ignore_value="0xFFFFFFFF"), img, 4, 8, -1)
+    if name == "c4rgb":             # the sheet as packed 24-bit RGB (2.4 GB)
+        img = wl.c4_sheet_rgb(device=device)
+        return (dict(workload="c4_sheet_24000x33600_rgb24", batch=1, H=wl.C4_H, W=wl.C4_W,
+                     pixel_bytes=3, connectivity=8, mode="all"), img, 3, 8, 0)
     if name.startswith("c4:"):      # the sheet generator at another size, e.g. c4:6000x8400
         H, W = (int(v) for v in name[3:].split("x"))
         img = wl.c4_sheet(device=device, H=H, W=W)
@@ -471,16 +475,20 @@ def main():
     if rank == 0 and world == 1 and not args.no_cpu_baseline and args.workload.startswith("c4"):
         import oracle
         oracle.build()
-        band = img[:CPU_BASELINE_ROWS].cpu().numpy().view(np.uint32)
+        if pb == 3:   # [1, H, W, 3] bytes
+            band = img[:, :CPU_BASELINE_ROWS].cpu().numpy()
+        else:
+            band = img[:CPU_BASELINE_ROWS].cpu().numpy().view(np.uint32)
         if mode < 0:
             t0 = time.perf_counter()
             oracle.label_ignore(band, int(cfg["ignore_value"], 16), 8)
             dt = time.perf_counter() - t0
         else:
             dt = time_oracle(band, 8, oracle.MODE_ALL)
-        cpu_baseline = {"value": band.size / dt / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
+        band_px = band.size // 3 if pb == 3 else band.size
+        cpu_baseline = {"value": band_px / dt / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
                         "sample": "rows 0-%d of the sheet (%d px), one single-threaded BFS pass, "
-                                  "%.1f s" % (CPU_BASELINE_ROWS, band.size, dt)}
+                                  "%.1f s" % (CPU_BASELINE_ROWS, band_px, dt)}
 
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
