@@ -264,7 +264,7 @@ int run_pipeline(const void* img, int batch, int H, int W, int pb, int conn, int
   k_resolve<<<(unsigned)((L.nTiles + NWARPS - 1) / NWARPS), NT, 0, st>>>(bd, L.nTiles, labels, bm, cnt,
                                                                           g, capImg, status);
   mark(4);
-  k_number<<<grid, NT, 0, st>>>(L16, labels, bm, cnt, g, status);
+  k_number<<<grid, NT, 0, st>>>(L16, labels, bm, cnt, bd, g, status);
   mark(5);
   if (timed) keep_event_set(es);
   g_launches += n_out ? 8 : 7;

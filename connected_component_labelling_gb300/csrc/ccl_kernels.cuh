@@ -941,17 +941,20 @@ __global__ void __launch_bounds__(NT, 8) k_resolve(Border bd, long long nTiles, 
   }
 }
 
-// Number: labels of the tile's leaders (from the bitmap and the chunk
-// offsets, or, for leaders re-pointed across a seam, the negated label
-// k_resolve left in their slot), then every pixel takes the label of its
-// tile-local leader, two hops away in the leader map.  The labels buffer holds the slots of border leaders
-// until this kernel overwrites it; a tile reads only its own slots, before
-// writing.
+// Number: labels of the tile's leaders -- from the bitmap and the chunk
+// offsets, or, for leaders re-pointed across a seam (all of them are in the
+// tile's border list), the negated label k_resolve left in their slot --
+// then every pixel takes the label of its tile-local leader, two hops away in
+// the leader map.  The labels buffer holds the slots of border leaders until
+// this kernel overwrites it; a tile reads only its own slots, before writing.
+// Both lookup tables end in a sentinel entry (index TILE: map -> TILE, label
+// 0), which background and any out-of-range entry are clamped to.
 __global__ void __launch_bounds__(NT, 8) k_number(const uint16_t* __restrict__ L16, int32_t* labels,
                                                const uint32_t* __restrict__ bm,
-                                               const uint32_t* __restrict__ off, Geom g, int* status) {
-  __shared__ __align__(16) int lab[TILE];
-  __shared__ __align__(16) uint16_t lmap[TILE];   // the tile's leader map
+                                               const uint32_t* __restrict__ off, Border bd, Geom g,
+                                               int* status) {
+  __shared__ __align__(16) int lab[TILE + 1];
+  __shared__ __align__(16) uint16_t lmap[TILE + 8];   // the tile's leader map
   const TileCoord t = tile_coord(g);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, xl = lane * PX;
   const long long ioff = (long long)t.b * g.HW;
@@ -962,6 +965,10 @@ __global__ void __launch_bounds__(NT, 8) k_number(const uint16_t* __restrict__ L
   const uint32_t base0 = offi[0];
   const int nval = max(0, min(PX, t.tw - xl));
   const bool vec = g.vec_out && nval == PX;
+  if (threadIdx.x == 0) {
+    lab[TILE] = 0;
+    lmap[TILE] = (uint16_t)TILE;
+  }
   uint32_t lw[RPW][PX / 2];   // the lane's 8 leader-map entries per row, two per word
 
 #pragma unroll
@@ -995,23 +1002,26 @@ __global__ void __launch_bounds__(NT, 8) k_number(const uint16_t* __restrict__ L
     const uint32_t pre = __shfl_sync(FULL, inc - mine, lane & ~3);
     const uint32_t o = offi[(long long)(t.y0 + r) * g.CPR + t.tx] - base0;
     const int i0 = r * TW + xl;
-    unsigned lead = 0;   // pixels of this lane that are their own tile-local leader
-#pragma unroll
-    for (int j = 0; j < PX; ++j)
-      lead |= (((lw[k][j >> 1] >> (16 * (j & 1))) & 0xFFFFu) == (uint32_t)(i0 + j)) ? (1u << j) : 0u;
-    const unsigned wbits = (w >> ((xl & 31))) & 0xFFu;
-    unsigned m = lead;
+    // the bitmap's leaders among this lane's pixels: 1 + leaders before them
+    unsigned m = (w >> (xl & 31)) & 0xFFu;
     while (m) {
       const int j = __ffs(m) - 1;
       m &= m - 1;
-      if ((wbits >> j) & 1u) {
-        const int bit = (xl + j) & 31;
-        lab[i0 + j] = (int)(o + pre + __popc(w & ((1u << bit) - 1u)) + 1u);
-      } else {
-        const int v = Pi[(long long)(t.y0 + r) * g.W + t.x0 + xl + j];
-        if (v >= 0) raise_flag(status, FLAG_INTERNAL);
-        lab[i0 + j] = v < 0 ? -v : 0;
-      }
+      const int bit = (xl + j) & 31;
+      lab[i0 + j] = (int)(o + pre + __popc(w & ((1u << bit) - 1u)) + 1u);
+    }
+  }
+  // leaders re-pointed across a seam: the label k_resolve stored, negated
+  {
+    const long long tile = blockIdx.x;
+    const int count = min((int)bd.cnt[tile], BLCAP);
+    const uint16_t* list = bd.list + tile * BLCAP;
+    for (int q = threadIdx.x; q < count; q += NT) {
+      const int l = list[q];
+      const int gi = (t.y0 + (l >> LOG_TW)) * g.W + t.x0 + (l & (TW - 1));
+      const int v = Pi[gi];
+      if (v < 0) lab[l & (TILE - 1)] = -v;
+      else if (v != gi) raise_flag(status, FLAG_INTERNAL);   // neither leader nor resolved
     }
   }
   __syncthreads();
@@ -1023,9 +1033,8 @@ __global__ void __launch_bounds__(NT, 8) k_number(const uint16_t* __restrict__ L
 #pragma unroll
     for (int j = 0; j < PX; ++j) {
       // pixel -> run start -> leader
-      const uint32_t l = (lw[k][j >> 1] >> (16 * (j & 1))) & 0xFFFFu;
-      const uint32_t ld = l < (uint32_t)TILE ? (uint32_t)lmap[l] : 0xFFFFu;
-      out[j] = ld < (uint32_t)TILE ? lab[ld] : 0;
+      const uint32_t l = min((lw[k][j >> 1] >> (16 * (j & 1))) & 0xFFFFu, (uint32_t)TILE);
+      out[j] = lab[min((uint32_t)lmap[l], (uint32_t)TILE)];
     }
     int32_t* orow = Pi + (long long)(t.y0 + r) * g.W + t.x0 + xl;
     if (vec) {
