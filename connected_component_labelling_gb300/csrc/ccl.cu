@@ -261,7 +261,7 @@ int run_pipeline(const void* img, int batch, int H, int W, int pb, int conn, int
   if (n_out)
     k_region_counts<<<(batch + 255) / 256, 256, 0, st>>>(cnt, (long long)H * L.g.CPR, batch, n_out);
   mark(3);
-  k_resolve<<<(unsigned)((L.nTiles + NWARPS - 1) / NWARPS), NT, 0, st>>>(bd, L.nTiles, labels, bm, cnt,
+  k_resolve<<<(unsigned)((L.nTiles + RESOLVE_WARPS - 1) / RESOLVE_WARPS), 32 * RESOLVE_WARPS, 0, st>>>(bd, L.nTiles, labels, bm, cnt,
                                                                           g, capImg, status);
   mark(4);
   k_number<<<grid, NT, 0, st>>>(L16, labels, bm, cnt, bd, g, status);

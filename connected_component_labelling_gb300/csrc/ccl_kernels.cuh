@@ -621,11 +621,11 @@ __global__ void __launch_bounds__(NT, 8) k_tile_local(const T* __restrict__ img,
 // keeps every distinct pair of leaders to join once (a small hash set: along
 // a seam many joins link the same two regions), then its lanes unite the
 // kept pairs side by side.
-constexpr int SEAM_WARPS = 4;
+constexpr int SEAM_WARPS = 2;
 constexpr int SEAM_HASH = 128;
 
 template <typename T, int CONN, bool BIN>
-__global__ void __launch_bounds__(32 * SEAM_WARPS, 16) k_seams(const T* __restrict__ img,
+__global__ void __launch_bounds__(32 * SEAM_WARPS, 32) k_seams(const T* __restrict__ img,
                                                                const uint16_t* __restrict__ L16, int32_t* P,
                                                                uint32_t* bm, uint32_t* cnt, Border bd, Geom g,
                                                                long long nTiles, int cap, int* status) {
@@ -888,25 +888,31 @@ __device__ __forceinline__ int number_of(int gidx, const uint32_t* bmi, const ui
   }
   const int gy = div_w(gidx, g), gx = gidx - gy * g.W;
   const long long w0 = (long long)gy * g.WPR + ((gx >> LOG_TW) << 3);
-  const long long wg = (long long)gy * g.WPR + (gx >> 5);
+  const int nw = (gx >> 5) & 7;   // whole words of the chunk before the leader's word
+  // every load of the chunk's words is issued before any is used
+  const uint32_t chunk = offi[(long long)gy * g.CPR + (gx >> LOG_TW)];
+  const uint32_t word = bmi[w0 + nw];
   uint32_t s = 0;
-  for (long long w = w0; w < wg; ++w) s += __popc(bmi[w]);
-  const uint32_t word = bmi[wg];
+#pragma unroll
+  for (int k = 0; k < 7; ++k)
+    if (k < nw) s += __popc(bmi[w0 + k]);
   if (!((word >> (gx & 31)) & 1u)) raise_flag(status, FLAG_INTERNAL);
   s += __popc(word & ((1u << (gx & 31)) - 1u));
-  return (int)(offi[(long long)gy * g.CPR + (gx >> LOG_TW)] - base0 + s + 1u);
+  return (int)(chunk - base0 + s + 1u);
 }
+
+constexpr int RESOLVE_WARPS = 2;   // tiles (a warp each) per block: small blocks free their slot sooner
 
 // Collapse + Number for the leaders re-pointed across seams, taken from the
 // tiles' border lists (a warp per tile).  Each walks to its final leader
 // (halving on the way), takes that leader's label and stores it negated in
 // its own slot.  A walk that meets a slot already holding a negated label
 // stops there: every node on a walk belongs to the same region.
-__global__ void __launch_bounds__(NT, 8) k_resolve(Border bd, long long nTiles, int32_t* P,
+__global__ void __launch_bounds__(32 * RESOLVE_WARPS, 32) k_resolve(Border bd, long long nTiles, int32_t* P,
                                                 const uint32_t* __restrict__ bm,
                                                 const uint32_t* __restrict__ off, Geom g, int cap,
                                                 int* status) {
-  const long long tile = (long long)blockIdx.x * NWARPS + (threadIdx.x >> 5);
+  const long long tile = (long long)blockIdx.x * RESOLVE_WARPS + (threadIdx.x >> 5);
   if (tile >= nTiles) return;
   const int lane = threadIdx.x & 31;
   const TileCoord t = tile_coord_of(g, tile);
