@@ -335,19 +335,14 @@ __device__ __forceinline__ int leader_of(const uint16_t* Li, int y, int x, const
   return ly * g.W + lx;
 }
 
-__device__ __forceinline__ int warp_sum(int v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(FULL, v, o);
-  return v;
-}
-
 // ------------------------------------------------------------------ kernels
 
 // Occupancy matters more than a few spilled registers here: the in-tile
 // union-find is latency-bound, so the kernel is held to 32 registers (8
 // blocks of 256 threads per SM) and keeps no copy of the image in shared
-// memory (Connect re-reads the two rows it compares; a sibling warp of the
-// block has just loaded them, so they come from L1).
+// memory: Start compares each row with the row above while both are in
+// registers (the row above was just loaded by a sibling warp: an L1 or L2
+// hit) and keeps only the join bits for Connect.
 template <typename T, int CONN, bool BIN>
 __global__ void __launch_bounds__(NT, 8) k_tile_local(const T* __restrict__ img, uint16_t* __restrict__ L16,
                                                    int32_t* __restrict__ P, uint32_t* __restrict__ bm,
@@ -374,7 +369,7 @@ __global__ void __launch_bounds__(NT, 8) k_tile_local(const T* __restrict__ img,
   // per row of this warp: foreground pixels, pixels equal to their left
   // neighbour (same run), and the row position of the last run start left
   // of this lane
-  unsigned fgm[RPW], eqm[RPW];
+  unsigned fgm[RPW], eqm[RPW], tdm[RPW];
   int befm[RPW];
 
   // ---- Start: every pixel points at the first pixel of its run
@@ -383,6 +378,7 @@ __global__ void __launch_bounds__(NT, 8) k_tile_local(const T* __restrict__ img,
     const int r = warp + k * NWARPS;
     fgm[k] = 0;
     eqm[k] = 0;
+    tdm[k] = 0;
     befm[k] = -1;
     if (r >= t.th) continue;   // warp-uniform
     uint32_t c[PX];
@@ -400,20 +396,43 @@ __global__ void __launch_bounds__(NT, 8) k_tile_local(const T* __restrict__ img,
     for (int j = 1; j < PX; ++j) eq |= (c[j] == c[j - 1] ? 1u : 0u) << j;
     eq &= fg & (fg << 1 | 1u);
     const unsigned starts = fg & ~eq;
-    int last = starts ? xl + 31 - __clz(starts) : -1;
+    // the joins with the row above (Connect makes them): this row's pixels
+    // against the row above, while they are in registers
+    if (r > 0) {   // warp-uniform
+      uint32_t u[PX];
+      load8<T>(im + (long long)(t.y0 + r - 1) * g.W + t.x0 + xl, vec, nval, u);
+      const uint32_t uL = __shfl_up_sync(FULL, u[PX - 1], 1);
+      const uint32_t uR = __shfl_down_sync(FULL, u[0], 1);
+      unsigned mU = 0, mUL = 0, mUR = 0;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(FULL, last, o);
-      if (lane >= o) last = max(last, y);
+      for (int j = 0; j < PX; ++j) {
+        const uint32_t cj = c[j];
+        mU |= (cj == u[j] ? 1u : 0u) << j;
+        mUL |= (j > 0 ? cj == u[j - 1] : (lane > 0 && cj == uL)) ? (1u << j) : 0u;
+        if (CONN == 8)
+          mUR |= (j < PX - 1 ? cj == u[j + 1] : (lane < 31 && cj == uR)) ? (1u << j) : 0u;
+      }
+      mU &= fg;
+      mUL &= fg;
+      mUR &= fg & ((vmask >> 1) | ((lane < 31 && xl + PX < t.tw) ? 0x80u : 0u));
+      if (CONN == 8)
+        tdm[k] = (mU & ~eq) | ((mUL & ~mU & ~eq) << 8) | ((mUR & ~mU) << 16);
+      else
+        tdm[k] = mU & ~(eq & mUL);
     }
-    int cur = __shfl_up_sync(FULL, last, 1);
-    if (lane == 0) cur = -1;
+    // the last run start left of this lane: the last start of the nearest
+    // lane on the left that has one
+    const unsigned left = __ballot_sync(FULL, starts != 0u) & ((1u << lane) - 1u);
+    int cur = __shfl_sync(FULL, xl + 31 - __clz(starts), 31 - __clz(left | 1u));
+    if (!left) cur = -1;
     befm[k] = cur;
+    // (all-pixels mode: every pixel of the lane is foreground; the entries
+    // past the tile's last column are never read)
     int pv[PX];
 #pragma unroll
     for (int j = 0; j < PX; ++j) {
       if ((starts >> j) & 1u) cur = xl + j;
-      pv[j] = ((fg >> j) & 1u) ? r * TW + cur : -1;
+      pv[j] = (!BIN || ((fg >> j) & 1u)) ? r * TW + cur : -1;
     }
     int4* pp = reinterpret_cast<int4*>(par + r * TW + xl);
     pp[0] = make_int4(pv[0], pv[1], pv[2], pv[3]);
@@ -423,8 +442,9 @@ __global__ void __launch_bounds__(NT, 8) k_tile_local(const T* __restrict__ img,
     uint32_t lw[PX / 2];
 #pragma unroll
     for (int q = 0; q < PX / 2; ++q)
-      lw[q] = (pv[2 * q] < 0 ? LBG : (uint32_t)pv[2 * q]) |
-              ((pv[2 * q + 1] < 0 ? LBG : (uint32_t)pv[2 * q + 1]) << 16);
+      lw[q] = BIN ? ((pv[2 * q] < 0 ? LBG : (uint32_t)pv[2 * q]) |
+                     ((pv[2 * q + 1] < 0 ? LBG : (uint32_t)pv[2 * q + 1]) << 16))
+                  : ((uint32_t)pv[2 * q] | ((uint32_t)pv[2 * q + 1] << 16));
     uint16_t* lrow = Li + (long long)(t.y0 + r) * g.W + t.x0 + xl;
     if (g.vec_out && nval == PX) {
       *reinterpret_cast<uint4*>(lrow) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
@@ -442,41 +462,13 @@ __global__ void __launch_bounds__(NT, 8) k_tile_local(const T* __restrict__ img,
   // join goes to the row above; a pixel equal to its left neighbour leaves
   // up-left and up to it (8-connectivity), or up when up-left matches too
   // (4-connectivity).  Neighbours outside the tile count as absent here;
-  // k_seams makes those joins.
+  // k_seams makes those joins.  Start found the joins (tdm: bit j up, j+8
+  // up-left, j+16 up-right of the lane's pixel j).
 #pragma unroll
   for (int k = 0; k < RPW; ++k) {
     const int r = warp + k * NWARPS;
     if (r >= t.th || r == 0) continue;   // warp-uniform
-    uint32_t c[PX], u[PX];
-    // this row and the row above, again from the image (a sibling warp of
-    // this block has just read them: L1 hits)
-    load8<T>(im + (long long)(t.y0 + r) * g.W + t.x0 + xl, vec, nval, c);
-    load8<T>(im + (long long)(t.y0 + r - 1) * g.W + t.x0 + xl, vec, nval, u);
-    const uint32_t uL = __shfl_up_sync(FULL, u[PX - 1], 1);
-    const uint32_t uR = __shfl_down_sync(FULL, u[0], 1);
-    const unsigned fg = fgm[k], eq = eqm[k];
-    unsigned mU = 0, mUL = 0, mUR = 0;
-#pragma unroll
-    for (int j = 0; j < PX; ++j) {
-      const uint32_t cj = c[j];
-      mU |= (cj == u[j] ? 1u : 0u) << j;
-      mUL |= (j > 0 ? cj == u[j - 1] : (lane > 0 && cj == uL)) ? (1u << j) : 0u;
-      if (CONN == 8)
-        mUR |= (j < PX - 1 ? cj == u[j + 1] : (lane < 31 && cj == uR)) ? (1u << j) : 0u;
-    }
-    mU &= fg;   // the pixel above is in the tile whenever this one is
-    mUL &= fg;
-    // up-right exists when the column to the right is in the tile
-    mUR &= fg & ((vmask >> 1) | ((lane < 31 && xl + PX < t.tw) ? 0x80u : 0u));
-    unsigned todo;
-    if (CONN == 8) {
-      const unsigned jU = mU & ~eq;
-      const unsigned jUL = mUL & ~mU & ~eq;
-      const unsigned jUR = mUR & ~mU;
-      todo = jU | (jUL << 8) | (jUR << 16);
-    } else {
-      todo = mU & ~(eq & mUL);
-    }
+    unsigned todo = tdm[k];
     const int i0 = r * TW + xl;
     // A lane walks its own joins one after another, so a warp loops as often
     // as its busiest lane.  When some lane has more than one join, the row's
@@ -568,8 +560,8 @@ __global__ void __launch_bounds__(NT, 8) k_tile_local(const T* __restrict__ img,
     const unsigned b3 = __shfl_down_sync(FULL, rm, 3);
     if ((lane & 3) == 0 && xl < t.tw)
       bmi[(long long)(t.y0 + r) * g.WPR + ((t.x0 + xl) >> 5)] = rm | (b1 << 8) | (b2 << 16) | (b3 << 24);
-    const int n = warp_sum(__popc(rm));
-    if (lane == 0) cnti[(long long)(t.y0 + r) * g.CPR + t.tx] = (uint32_t)n;
+    const unsigned n = __reduce_add_sync(FULL, (unsigned)__popc(rm));
+    if (lane == 0) cnti[(long long)(t.y0 + r) * g.CPR + t.tx] = n;
   }
   __syncthreads();
 
