@@ -988,16 +988,17 @@ __global__ void __launch_bounds__(NT, 8) k_number(const uint16_t* __restrict__ L
       }
     }
     *reinterpret_cast<uint4*>(lmap + r * TW + xl) = make_uint4(lw[k][0], lw[k][1], lw[k][2], lw[k][3]);
-    // word w of the row segment belongs to lanes 4w..4w+3; lane 4w counts it
+    // word w of the row segment belongs to lanes 4w..4w+3, which all hold it:
+    // leaders in the words before it, by a scan over the 8 words
     const uint32_t w = xl < t.tw ? bmi[(long long)(t.y0 + r) * g.WPR + ((t.x0 + xl) >> 5)] : 0u;
-    const uint32_t mine = ((lane & 3) == 0) ? __popc(w) : 0u;
-    uint32_t inc = mine;
+    const uint32_t cw = __popc(w);
+    uint32_t inc = cw;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
+    for (int o = 4; o < 32; o <<= 1) {
       const uint32_t y = __shfl_up_sync(FULL, inc, o);
       if (lane >= o) inc += y;
     }
-    const uint32_t pre = __shfl_sync(FULL, inc - mine, lane & ~3);
+    const uint32_t pre = inc - cw;
     const uint32_t o = offi[(long long)(t.y0 + r) * g.CPR + t.tx] - base0;
     const int i0 = r * TW + xl;
     // the bitmap's leaders among this lane's pixels: 1 + leaders before them
