@@ -277,6 +277,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-stats", action="store_true",
                     help="skip timing ccl_region_stats on the labels")
+    ap.add_argument("--counters", action="store_true",
+                    help="also label the workload once with the counters build of the library "
+                         "and report walks, steps per walk and links (not timed)")
     ap.add_argument("--ref-rows", type=int, default=REF_ROWS,
                     help="rows of the sheet one reference (oracle) step labels")
     args = ap.parse_args()
@@ -443,6 +446,26 @@ def main():
                                 "3 kernel launches per call"}
         del sraw, sws
 
+    # ---- event counters: one untimed call through the counters build
+    counters = None
+    if args.counters and rank == 0:
+        CL = ccl.counters_library()
+        ccl.read_counters(CL, reset=True)
+        if mode < 0:
+            rc = CL.ccl_label_ignore(img.data_ptr(), B, H, W, pb, conn, int(cfg["ignore_value"], 16),
+                                     labels.data_ptr(), nreg.data_ptr(), ws.data_ptr(), wsb, sp)
+        else:
+            rc = CL.ccl_label_ws(img.data_ptr(), B, H, W, pb, conn, mode, labels.data_ptr(),
+                                 nreg.data_ptr(), ws.data_ptr(), wsb, sp)
+        if rc != ccl.CCL_OK:
+            raise ccl.CCLError(rc, "counters build")
+        c = ccl.read_counters(CL, reset=True)
+        counters = dict(c)
+        counters["tile_steps_per_walk"] = c["tile_steps"] / max(1, c["tile_walks"])
+        counters["global_steps_per_walk"] = c["global_steps"] / max(1, c["global_walks"])
+        counters["tile_links_per_px"] = c["tile_links"] / px
+        counters["build"] = "libccl_counters.so (-DCCL_COUNTERS), one call, not timed"
+
     # ---- e2e through the host entry point
     e2e = None
     if not args.no_e2e and mode >= 0:
@@ -501,7 +524,7 @@ def main():
                                parallelism="replicas" if world > 1 else "single"),
                 "roofline": roofline, "roofline_path": roofline_path, "stages": stages,
                 "cpu_baseline": cpu_baseline, "e2e": e2e, "gpu_launches": launches,
-                "region_stats": region_stats,
+                "region_stats": region_stats, "counters": counters,
                 "clocks": clocks, "n_regions": n_regions[:8],
                 "kernel_source_sha": source_sha()}
         print(json.dumps(line), flush=True)

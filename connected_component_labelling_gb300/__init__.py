@@ -15,7 +15,7 @@ import ctypes
 import os
 import threading
 
-from ._build import LIB_PATH, build  # noqa: F401
+from ._build import COUNTERS_LIB_PATH, LIB_PATH, build  # noqa: F401
 
 CCL_OK = 0
 CCL_ERR_INVALID_ARG = 1
@@ -32,7 +32,12 @@ CCL_OPT_STAGE_EVENTS = 2
 EXPORTED = ("ccl_label", "ccl_workspace_bytes", "ccl_label_ws", "ccl_label_host",
             "ccl_last_status", "ccl_status_string", "ccl_set_option", "ccl_stage_times",
             "ccl_stage_name", "ccl_kernel_launches", "ccl_label_noalloc", "ccl_label_ignore",
-            "ccl_region_stats_workspace_bytes", "ccl_region_stats", "ccl_version")
+            "ccl_region_stats_workspace_bytes", "ccl_region_stats", "ccl_debug_counters",
+            "ccl_version")
+
+# event counters of the counters build (include/ccl.h, CCL_CNT_*)
+COUNTER_NAMES = ("tile_walks", "tile_steps", "tile_links", "global_walks", "global_steps",
+                 "global_links", "seam_pairs", "resolve_steps")
 
 # one region's statistics (struct ccl_region_stat, 40 bytes): six int32 then two int64
 STAT_BYTES = 40
@@ -49,6 +54,45 @@ class CCLError(RuntimeError):
         super().__init__("%s%s" % (what + ": " if what else "", ccl_status_string(status)))
 
 
+def _declare(L):
+    """Argument and result types of every entry point of a loaded library."""
+    vp, i32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+    L.ccl_label.argtypes = [vp, i32, i32, i32, i32, i32, i32, vp, vp, vp]
+    L.ccl_label.restype = i32
+    L.ccl_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, i32]
+    L.ccl_workspace_bytes.restype = sz
+    L.ccl_label_ws.argtypes = [vp, i32, i32, i32, i32, i32, i32, vp, vp, vp, sz, vp]
+    L.ccl_label_ws.restype = i32
+    L.ccl_label_host.argtypes = [vp, i32, i32, i32, i32, i32, i32, vp, vp, vp]
+    L.ccl_label_host.restype = i32
+    L.ccl_last_status.argtypes = [vp]
+    L.ccl_last_status.restype = i32
+    L.ccl_status_string.argtypes = [i32]
+    L.ccl_status_string.restype = ctypes.c_char_p
+    L.ccl_set_option.argtypes = [i32, ctypes.c_longlong]
+    L.ccl_set_option.restype = i32
+    L.ccl_stage_times.argtypes = [vp, i32, vp]
+    L.ccl_stage_times.restype = i32
+    L.ccl_stage_name.argtypes = [i32]
+    L.ccl_stage_name.restype = ctypes.c_char_p
+    L.ccl_kernel_launches.argtypes = []
+    L.ccl_kernel_launches.restype = ctypes.c_longlong
+    L.ccl_label_noalloc.argtypes = [vp, i32, i32, i32, i32, i32, i32, vp, vp, vp]
+    L.ccl_label_noalloc.restype = i32
+    L.ccl_label_ignore.argtypes = [vp, i32, i32, i32, i32, i32, ctypes.c_uint32, vp, vp,
+                                   vp, sz, vp]
+    L.ccl_label_ignore.restype = i32
+    L.ccl_region_stats_workspace_bytes.argtypes = [i32]
+    L.ccl_region_stats_workspace_bytes.restype = sz
+    L.ccl_region_stats.argtypes = [vp, i32, i32, i32, vp, vp, ctypes.c_int64, vp, sz, vp]
+    L.ccl_region_stats.restype = i32
+    L.ccl_version.argtypes = []
+    L.ccl_version.restype = i32
+    L.ccl_debug_counters.argtypes = [vp, i32, i32]
+    L.ccl_debug_counters.restype = i32
+    return L
+
+
 def lib():
     """The loaded libccl.so (raises if it has not been built)."""
     global _lib
@@ -57,39 +101,7 @@ def lib():
             if not os.path.exists(LIB_PATH):
                 raise RuntimeError("libccl.so is not built (%s); run "
                                    "connected_component_labelling_gb300.build()" % LIB_PATH)
-            L = ctypes.CDLL(LIB_PATH)
-            vp, i32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
-            L.ccl_label.argtypes = [vp, i32, i32, i32, i32, i32, i32, vp, vp, vp]
-            L.ccl_label.restype = i32
-            L.ccl_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, i32]
-            L.ccl_workspace_bytes.restype = sz
-            L.ccl_label_ws.argtypes = [vp, i32, i32, i32, i32, i32, i32, vp, vp, vp, sz, vp]
-            L.ccl_label_ws.restype = i32
-            L.ccl_label_host.argtypes = [vp, i32, i32, i32, i32, i32, i32, vp, vp, vp]
-            L.ccl_label_host.restype = i32
-            L.ccl_last_status.argtypes = [vp]
-            L.ccl_last_status.restype = i32
-            L.ccl_status_string.argtypes = [i32]
-            L.ccl_status_string.restype = ctypes.c_char_p
-            L.ccl_set_option.argtypes = [i32, ctypes.c_longlong]
-            L.ccl_set_option.restype = i32
-            L.ccl_stage_times.argtypes = [vp, i32, vp]
-            L.ccl_stage_times.restype = i32
-            L.ccl_stage_name.argtypes = [i32]
-            L.ccl_stage_name.restype = ctypes.c_char_p
-            L.ccl_kernel_launches.argtypes = []
-            L.ccl_kernel_launches.restype = ctypes.c_longlong
-            L.ccl_label_noalloc.argtypes = [vp, i32, i32, i32, i32, i32, i32, vp, vp, vp]
-            L.ccl_label_noalloc.restype = i32
-            L.ccl_label_ignore.argtypes = [vp, i32, i32, i32, i32, i32, ctypes.c_uint32, vp, vp,
-                                           vp, sz, vp]
-            L.ccl_label_ignore.restype = i32
-            L.ccl_region_stats_workspace_bytes.argtypes = [i32]
-            L.ccl_region_stats_workspace_bytes.restype = sz
-            L.ccl_region_stats.argtypes = [vp, i32, i32, i32, vp, vp, ctypes.c_int64, vp, sz, vp]
-            L.ccl_region_stats.restype = i32
-            L.ccl_version.argtypes = []
-            L.ccl_version.restype = i32
+            L = _declare(ctypes.CDLL(LIB_PATH))
             _lib = L
     return _lib
 
@@ -238,6 +250,26 @@ def region_stats(labels, n_regions, capacity=None, workspace=None, stream=None):
     fields = {f: i32[:, k] for k, f in enumerate(STAT_FIELDS_I32)}
     fields.update({f: i64[:, 3 + k] for k, f in enumerate(STAT_FIELDS_I64)})
     return raw, fields
+
+
+def ccl_debug_counters(out, n, reset):
+    return lib().ccl_debug_counters(out, n, reset)
+
+
+def counters_library():
+    """The counters build of the library (built on first use): a separate
+    libccl_counters.so with event counters compiled in, for measuring the
+    method (bench.py --counters).  Same entry points as ``lib()``."""
+    return _declare(ctypes.CDLL(build(counters=True)))
+
+
+def read_counters(L, reset=True):
+    """The event counters of library ``L`` as a dict (COUNTER_NAMES)."""
+    buf = (ctypes.c_ulonglong * len(COUNTER_NAMES))()
+    rc = L.ccl_debug_counters(buf, len(COUNTER_NAMES), 1 if reset else 0)
+    if rc != CCL_OK:
+        raise CCLError(rc, "ccl_debug_counters")
+    return dict(zip(COUNTER_NAMES, (int(v) for v in buf)))
 
 
 def ccl_version():

@@ -10,6 +10,9 @@ SRC = [os.path.join(HERE, "csrc", "ccl.cu")]
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(BUILD_DIR, "libccl.so")
+# the same library with event counters compiled in (ccl_debug_counters); never
+# the one the product path loads
+COUNTERS_LIB_PATH = os.path.join(BUILD_DIR, "libccl_counters.so")
 
 NVCC_FLAGS = ["-std=c++17", "-O3", "-gencode", "arch=compute_103a,code=sm_103a",
               "-lineinfo", "-Xcompiler", "-fPIC", "-shared"]
@@ -22,24 +25,27 @@ def _nvcc():
     return "nvcc"
 
 
-def _stale():
-    if not os.path.exists(LIB_PATH):
+def _stale(path):
+    if not os.path.exists(path):
         return True
-    t = os.path.getmtime(LIB_PATH)
+    t = os.path.getmtime(path)
     deps = SRC + [os.path.join(INCLUDE, "ccl.h")] + [
         os.path.join(HERE, "csrc", f) for f in os.listdir(os.path.join(HERE, "csrc"))]
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile csrc/*.cu into _build/libccl.so (skipped when up to date)."""
-    if not force and not _stale():
-        return LIB_PATH
+def build(force: bool = False, verbose: bool = False, counters: bool = False) -> str:
+    """Compile csrc/*.cu into _build/libccl.so (skipped when up to date); with
+    ``counters``, into _build/libccl_counters.so with the event counters on."""
+    path = COUNTERS_LIB_PATH if counters else LIB_PATH
+    if not force and not _stale(path):
+        return path
     os.makedirs(BUILD_DIR, exist_ok=True)
-    tmp = LIB_PATH + ".tmp%d" % os.getpid()
-    cmd = [_nvcc()] + NVCC_FLAGS + ["-I", INCLUDE, "-o", tmp] + SRC
+    tmp = path + ".tmp%d" % os.getpid()
+    cmd = [_nvcc()] + NVCC_FLAGS + (["-DCCL_COUNTERS"] if counters else []) + \
+        ["-I", INCLUDE, "-o", tmp] + SRC
     if verbose:
         print(" ".join(cmd))
     subprocess.check_call(cmd)
-    os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+    os.replace(tmp, path)
+    return path

@@ -508,6 +508,26 @@ int ccl_last_status(ccl_stream_t stream) {
   return CCL_OK;
 }
 
+int ccl_debug_counters(unsigned long long* out, int n, int reset) {
+#ifdef CCL_COUNTERS
+  if (!out || n < 0) return CCL_ERR_INVALID_ARG;
+  if (cudaDeviceSynchronize() != cudaSuccess) return CCL_ERR_CUDA;
+  unsigned long long h[CCL_NCOUNTERS];
+  if (cudaMemcpyFromSymbol(h, g_counters, sizeof(h)) != cudaSuccess) return CCL_ERR_CUDA;
+  for (int i = 0; i < n && i < CCL_NCOUNTERS; ++i) out[i] = h[i];
+  if (reset) {
+    const unsigned long long z[CCL_NCOUNTERS] = {0};
+    if (cudaMemcpyToSymbol(g_counters, z, sizeof(z)) != cudaSuccess) return CCL_ERR_CUDA;
+  }
+  return CCL_OK;
+#else
+  (void)out;
+  (void)n;
+  (void)reset;
+  return CCL_ERR_INVALID_ARG;   // not the counters build
+#endif
+}
+
 size_t ccl_region_stats_workspace_bytes(int batch) {
   if (batch < 0) return 0;
   return align_up((size_t)(batch + 1) * sizeof(long long), 256);

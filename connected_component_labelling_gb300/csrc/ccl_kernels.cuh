@@ -125,6 +125,17 @@ __device__ __forceinline__ int div_w(int d, const Geom& g) {
 
 __device__ __forceinline__ void raise_flag(int* status, int f) { atomicOr(status, f); }
 
+// Event counters, compiled in only for the counters build (-DCCL_COUNTERS;
+// read with ccl_debug_counters): walks and their steps in shared and global
+// memory, links, kept seam pairs and resolve steps.  Each event is one global
+// atomic, so that build is slow; the product build has none of it.
+#ifdef CCL_COUNTERS
+__device__ unsigned long long g_counters[CCL_NCOUNTERS];
+#define CCL_COUNT(i) atomicAdd(&g_counters[i], 1ull)
+#else
+#define CCL_COUNT(i) ((void)0)
+#endif
+
 // ---------------------------------------------------------------- pixel I/O
 // Eight consecutive pixels, widened to 32 bits.
 
@@ -237,7 +248,9 @@ __device__ __forceinline__ void ld8s<uint32_t>(const uint32_t* s, uint32_t c[PX]
 // volatile pointer so every step sees other threads' links.
 
 __device__ __forceinline__ int find_s(volatile int* par, int x, int cap, int* status) {
+  CCL_COUNT(CCL_CNT_TILE_WALKS);
   for (int s = 0; s < cap; ++s) {
+    CCL_COUNT(CCL_CNT_TILE_STEPS);
     const int p = par[x];
     if (p == x) return x;
     const int gp = par[p];
@@ -255,6 +268,7 @@ __device__ __forceinline__ void union_s(volatile int* par, int a, int b, int cap
     b = find_s(par, b, cap, status);
     if (a == b) return;
     if (a > b) { const int t = a; a = b; b = t; }
+    CCL_COUNT(CCL_CNT_TILE_LINKS);
     const int old = atomicMin((int*)&par[b], a);   // larger leader under smaller
     if (old == b) return;
     b = old;                                         // someone got there first
@@ -271,7 +285,9 @@ __device__ __forceinline__ void union_s(volatile int* par, int a, int b, int cap
 // walk in an earlier stage left a pixel pointing at a non-leader, whose slot
 // was never written, the walk stops with -1 instead of leaving the image.
 __device__ __forceinline__ int find_g(int* P, int x, int n, int cap, int* status) {
+  CCL_COUNT(CCL_CNT_GLOBAL_WALKS);
   for (int s = 0; s < cap; ++s) {
+    CCL_COUNT(CCL_CNT_GLOBAL_STEPS);
     const int p = __ldcg(P + x);
     if (p == x) return x;
     if ((unsigned)p >= (unsigned)n) {
@@ -306,6 +322,7 @@ __device__ __forceinline__ void union_g(int* P, int a, int b, uint32_t* bm, uint
     b = find_g(P, b, n, cap, status);
     if (a < 0 || b < 0 || a == b) return;
     if (a > b) { const int t = a; a = b; b = t; }
+    CCL_COUNT(CCL_CNT_GLOBAL_LINKS);
     const int old = atomicMin(P + b, a);
     if (old == b) {            // b stopped being a leader, exactly once
       drop_leader(b, bm, cnt, g);
@@ -722,6 +739,7 @@ __global__ void __launch_bounds__(32 * SEAM_WARPS, 32) k_seams(const T* __restri
     unsigned h = (unsigned)((key * 0x9E3779B97F4A7C15ull) >> 40) & (SEAM_HASH - 1);
     for (int probe = 0; probe < 8; ++probe) {
       const unsigned long long prev = atomicCAS(&seen[h], EMPTY, key);
+      if (prev == EMPTY) CCL_COUNT(CCL_CNT_SEAM_PAIRS);
       if (prev == EMPTY || prev == key) return;
       h = (h + 1) & (SEAM_HASH - 1);
     }
@@ -923,6 +941,7 @@ __global__ void __launch_bounds__(32 * RESOLVE_WARPS, 32) k_resolve(Border bd, l
     if (v == r || v < 0) continue;   // still a leader, or already resolved
     int node = r, lab = 0, s = 0;
     for (; s < cap; ++s) {
+      CCL_COUNT(CCL_CNT_RESOLVE_STEPS);
       const int p = __ldcg(Pi + node);
       if (p < 0) { lab = -p; break; }
       if (p == node) { lab = number_of(node, bmi, offi, base0, g, status); break; }
@@ -967,6 +986,15 @@ __global__ void __launch_bounds__(NT, 8) k_number(const uint16_t* __restrict__ L
     lab[TILE] = 0;
     lmap[TILE] = (uint16_t)TILE;
   }
+  // leaders re-pointed across a seam (all in the tile's border list) carry the
+  // label k_resolve stored, negated, in their slot: the list entry and then the
+  // slot are loaded first, so that both loads overlap the rows' work below
+  const long long tile = blockIdx.x;
+  const uint16_t* list = bd.list + tile * BLCAP;
+  const int count = min((int)bd.cnt[tile], BLCAP);
+  const int l0 = list[threadIdx.x];   // NT < BLCAP: always inside the tile's list
+  const int gi0 = (t.y0 + (l0 >> LOG_TW)) * g.W + t.x0 + (l0 & (TW - 1));
+  const int v0 = (int)threadIdx.x < count ? Pi[gi0] : 0;
   uint32_t lw[RPW][PX / 2];   // the lane's 8 leader-map entries per row, two per word
 
 #pragma unroll
@@ -1010,18 +1038,16 @@ __global__ void __launch_bounds__(NT, 8) k_number(const uint16_t* __restrict__ L
       lab[i0 + j] = (int)(o + pre + __popc(w & ((1u << bit) - 1u)) + 1u);
     }
   }
-  // leaders re-pointed across a seam: the label k_resolve stored, negated
-  {
-    const long long tile = blockIdx.x;
-    const int count = min((int)bd.cnt[tile], BLCAP);
-    const uint16_t* list = bd.list + tile * BLCAP;
-    for (int q = threadIdx.x; q < count; q += NT) {
-      const int l = list[q];
-      const int gi = (t.y0 + (l >> LOG_TW)) * g.W + t.x0 + (l & (TW - 1));
-      const int v = Pi[gi];
-      if (v < 0) lab[l & (TILE - 1)] = -v;
-      else if (v != gi) raise_flag(status, FLAG_INTERNAL);   // neither leader nor resolved
-    }
+  if ((int)threadIdx.x < count) {
+    if (v0 < 0) lab[l0 & (TILE - 1)] = -v0;
+    else if (v0 != gi0) raise_flag(status, FLAG_INTERNAL);   // neither leader nor resolved
+  }
+  for (int q = threadIdx.x + NT; q < count; q += NT) {   // lists longer than a block
+    const int l = list[q];
+    const int gi = (t.y0 + (l >> LOG_TW)) * g.W + t.x0 + (l & (TW - 1));
+    const int v = Pi[gi];
+    if (v < 0) lab[l & (TILE - 1)] = -v;
+    else if (v != gi) raise_flag(status, FLAG_INTERNAL);
   }
   __syncthreads();
 #pragma unroll

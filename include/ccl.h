@@ -255,6 +255,24 @@ int ccl_region_stats(const int32_t* labels_i32, int batch, int H, int W,
                      int64_t capacity, void* workspace, size_t workspace_bytes,
                      ccl_stream_t stream);
 
+/*
+ * Event counters of the labelling kernels, for measuring the method rather
+ * than using it: in-tile walks, their steps and links (shared memory),
+ * global walks, their steps and links (the parent array across tiles), seam
+ * leader pairs kept, resolve walk steps (indices CCL_CNT_*).  They exist only
+ * in the counters build of the library (compiled with -DCCL_COUNTERS, one
+ * global atomic per event, slow); the normal build returns
+ * CCL_ERR_INVALID_ARG.  ccl_debug_counters synchronises the device, copies
+ * min(n, CCL_NCOUNTERS) counters to `out` (host) and, if `reset`, zeroes them.
+ */
+#define CCL_NCOUNTERS 8
+enum {
+  CCL_CNT_TILE_WALKS = 0, CCL_CNT_TILE_STEPS = 1, CCL_CNT_TILE_LINKS = 2,
+  CCL_CNT_GLOBAL_WALKS = 3, CCL_CNT_GLOBAL_STEPS = 4, CCL_CNT_GLOBAL_LINKS = 5,
+  CCL_CNT_SEAM_PAIRS = 6, CCL_CNT_RESOLVE_STEPS = 7
+};
+int ccl_debug_counters(unsigned long long* out, int n, int reset);
+
 /* Library version, as major*10000 + minor*100 + patch. */
 int ccl_version(void);
 

@@ -158,3 +158,11 @@ def test_region_stats_host_checks(lib):
         ccl.CCL_ERR_TOO_LARGE
     assert ccl.ccl_region_stats(lab, 1, 8, 8, n, st, 10, ws + 16, 256, None) == ccl.CCL_ERR_INVALID_ARG
     assert ccl.ccl_region_stats(lab, 100, 8, 8, n, st, 10, ws, 512, None) == ccl.CCL_ERR_NO_MEMORY
+
+
+def test_counters_only_in_the_counters_build(lib):
+    import ctypes
+    buf = (ctypes.c_ulonglong * 8)()
+    # the product library has no counters compiled in
+    assert ccl.ccl_debug_counters(buf, 8, 0) == ccl.CCL_ERR_INVALID_ARG
+    assert len(ccl.COUNTER_NAMES) == 8
