@@ -12,7 +12,9 @@
 //                 the order of the joins" and switch 2, the Wu-Otoo-Suzuki
 //                 scan mask); walks halve paths with the same atomic minimum
 //                 (switch 3).  Output: a 2-byte leader map (a pixel's run
-//                 start; for a run start, its tile-local leader),
+//                 start; for a run start, its tile-local leader in the
+//                 tile's first and last rows and column 0, elsewhere an
+//                 ancestor on the way to it),
 //                 a leader bitmap, a leader count per 256-pixel chunk of a
 //                 row, and a global parent slot (its own raster index) for
 //                 every leader whose region touches the tile border.
@@ -29,7 +31,8 @@
 //                 its own slot.
 //   k_number      Number, last part: a leader's label is 1 + the number of
 //                 leaders before it in raster order; every pixel takes its
-//                 tile-local leader's label.
+//                 tile-local leader's label, finishing the walk in the leader
+//                 map (Collapse inside the tile is lazy: see k_tile_local).
 //
 // After labelling, on request (ccl_region_stats): region statistics --
 // area, bounding box, first pixel, coordinate sums -- as a reduction over the
@@ -333,9 +336,10 @@ __device__ __forceinline__ void union_g(int* P, int a, int b, uint32_t* bm, uint
   raise_flag(status, FLAG_WALK_CAP);
 }
 
-// image raster index of the tile-local leader of pixel (y, x), -1 for background
-// The leader map holds, for every pixel, its run start, and for every run
-// start its tile-local leader: two hops give the leader.
+// image raster index of the tile-local leader of pixel (y, x), -1 for background.
+// For a pixel in the first or last row of its tile: the leader map holds its
+// run start, and a run start of those rows holds its tile-local leader, so
+// two hops give the leader.  (k_seams asks only for such pixels.)
 __device__ __forceinline__ int leader_of(const uint16_t* Li, int y, int x, const Geom& g) {
   const int ty0 = y & ~(TH - 1), tx0 = x & ~(TW - 1);
   uint16_t l = Li[(long long)y * g.W + x];
@@ -454,22 +458,6 @@ __global__ void __launch_bounds__(NT, 8) k_tile_local(const T* __restrict__ img,
     int4* pp = reinterpret_cast<int4*>(par + r * TW + xl);
     pp[0] = make_int4(pv[0], pv[1], pv[2], pv[3]);
     pp[1] = make_int4(pv[4], pv[5], pv[6], pv[7]);
-    // leader map, first pass: every pixel's run start (background LBG);
-    // Collapse overwrites the entries of run starts with their leader
-    uint32_t lw[PX / 2];
-#pragma unroll
-    for (int q = 0; q < PX / 2; ++q)
-      lw[q] = BIN ? ((pv[2 * q] < 0 ? LBG : (uint32_t)pv[2 * q]) |
-                     ((pv[2 * q + 1] < 0 ? LBG : (uint32_t)pv[2 * q + 1]) << 16))
-                  : ((uint32_t)pv[2 * q] | ((uint32_t)pv[2 * q + 1] << 16));
-    uint16_t* lrow = Li + (long long)(t.y0 + r) * g.W + t.x0 + xl;
-    if (g.vec_out && nval == PX) {
-      *reinterpret_cast<uint4*>(lrow) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-    } else {
-#pragma unroll
-      for (int j = 0; j < PX; ++j)
-        if (j < nval) lrow[j] = (uint16_t)(lw[j >> 1] >> (16 * (j & 1)));
-    }
     fgm[k] = fg;
     eqm[k] = eq;
   }
@@ -512,7 +500,8 @@ __global__ void __launch_bounds__(NT, 8) k_tile_local(const T* __restrict__ img,
         const int j = bpos & 7;
         const int d = (bpos >> 3) == 0 ? 0 : ((bpos >> 3) == 1 ? -1 : 1);
         const int a = i0 + j, b = i0 + j - TW + d;
-        if (par[a] != par[b]) union_s(par, a, b, cap, status);   // else joined already
+        const int pa = par[a], pb = par[b];   // run starts (a pixel's entry never changes)
+        if (pa != pb) union_s(par, pa, pb, cap, status);   // else joined already
       }
     } else {
       while (todo) {
@@ -525,17 +514,21 @@ __global__ void __launch_bounds__(NT, 8) k_tile_local(const T* __restrict__ img,
         const int e = jlist[warp][q];
         const int a = e & (TILE - 1), dc = e >> 12;
         const int b = a - TW + (dc == 0 ? 0 : (dc == 1 ? -1 : 1));
-        if (par[a] != par[b]) union_s(par, a, b, cap, status);
+        const int pa = par[a], pb = par[b];
+        if (pa != pb) union_s(par, pa, pb, cap, status);
       }
       __syncwarp();
     }
   }
   __syncthreads();
 
-  // ---- Collapse inside the tile: one walk per run start.  The leader is
-  // stored back at the start (so par and the leader map give every pixel's
-  // leader in two hops: pixel -> run start -> leader); the leader bitmap,
-  // chunk counts and border marks follow from the starts alone
+  // ---- Collapse inside the tile, where it is read: the run starts of the
+  // tile's first and last rows (k_seams reads their leaders through the
+  // leader map), of column 0 and of the run holding the last column (border
+  // marks and records) walk to their leader and store it.  Every other start
+  // keeps the ancestor Connect left it; k_number finishes those walks.  The
+  // leader map of a row is then a copy of par: a pixel's run start, a start's
+  // leader or ancestor.  Leaders are the starts whose entry is themselves.
   unsigned rootm[RPW];
 #pragma unroll
   for (int k = 0; k < RPW; ++k) {
@@ -545,33 +538,57 @@ __global__ void __launch_bounds__(NT, 8) k_tile_local(const T* __restrict__ img,
     const unsigned starts = fgm[k] & ~eqm[k];
     const int i0 = r * TW + xl;
     const bool edgeRow = r == 0 || r == t.th - 1;
-    uint16_t* lrow = Li + (long long)(t.y0 + r) * g.W + t.x0 + xl;
-    unsigned m = starts, rm = 0;
+    unsigned m = edgeRow ? starts : (starts & (lane == 0 ? 1u : 0u));
     while (m) {
       const int j = __ffs(m) - 1;
       m &= m - 1;
       const int root = find_s(par, i0 + j, cap, status);
       par[i0 + j] = root;
-      if (root == i0 + j) rm |= 1u << j;
-      else lrow[j] = (uint16_t)root;
-      if (edgeRow || xl + j == 0) mark[root] = 1;
+      mark[root] = 1;
     }
-    rootm[k] = rm;
+    // the tile's right column: the leader of its run, marked
+    const int jr = t.tw - 1 - xl;
+    if (jr >= 0 && jr < PX && ((fgm[k] >> jr) & 1u)) {
+      const unsigned sm = starts & ((2u << jr) - 1u);
+      const int sr = r * TW + (sm ? xl + 31 - __clz(sm) : befm[k]);
+      const int root = find_s(par, sr, cap, status);
+      par[sr] = root;
+      mark[root] = 1;
+    }
   }
   __syncwarp();
 #pragma unroll
   for (int k = 0; k < RPW; ++k) {
     const int r = warp + k * NWARPS;
     if (r >= t.th) continue;   // warp-uniform
-    // the tile's right column: mark the leader of its run
-    const int jr = t.tw - 1 - xl;
-    const unsigned fg = fgm[k], starts = fg & ~eqm[k];
-    if (jr >= 0 && jr < PX && ((fg >> jr) & 1u)) {
-      const unsigned sm = starts & ((2u << jr) - 1u);
-      const int s = sm ? xl + 31 - __clz(sm) : befm[k];
-      mark[par[r * TW + s]] = 1;
+    const int i0 = r * TW + xl;
+    const int4 p0 = reinterpret_cast<const int4*>(par + i0)[0];
+    const int4 p1 = reinterpret_cast<const int4*>(par + i0)[1];
+    const int pj[PX] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+    const unsigned starts = fgm[k] & ~eqm[k];
+    unsigned rm = 0;
+    uint32_t lw[PX / 2];
+#pragma unroll
+    for (int j = 0; j < PX; ++j) {
+      rm |= (pj[j] == i0 + j) ? (1u << j) : 0u;
+      // a start that is not a leader: its grandparent (halves the walk left
+      // to k_number); any other pixel: its run start
+      int e = pj[j];
+      if (((starts >> j) & 1u) && e != i0 + j) e = par[e];
+      const uint32_t v = e < 0 ? (uint32_t)LBG : (uint32_t)e;
+      if (j & 1) lw[j >> 1] |= v << 16;
+      else lw[j >> 1] = v;
     }
-    const unsigned rm = rootm[k];
+    rm &= vmask;
+    rootm[k] = rm;
+    uint16_t* lrow = Li + (long long)(t.y0 + r) * g.W + t.x0 + xl;
+    if (g.vec_out && nval == PX) {
+      *reinterpret_cast<uint4*>(lrow) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+    } else {
+#pragma unroll
+      for (int j = 0; j < PX; ++j)
+        if (j < nval) lrow[j] = (uint16_t)(lw[j >> 1] >> (16 * (j & 1)));
+    }
     const unsigned b1 = __shfl_down_sync(FULL, rm, 1);
     const unsigned b2 = __shfl_down_sync(FULL, rm, 2);
     const unsigned b3 = __shfl_down_sync(FULL, rm, 3);
@@ -961,8 +978,8 @@ __global__ void __launch_bounds__(32 * RESOLVE_WARPS, 32) k_resolve(Border bd, l
 // Number: labels of the tile's leaders -- from the bitmap and the chunk
 // offsets, or, for leaders re-pointed across a seam (all of them are in the
 // tile's border list), the negated label k_resolve left in their slot --
-// then every pixel takes the label of its tile-local leader, two hops away in
-// the leader map.  The labels buffer holds the slots of border leaders until
+// then every pixel takes the label of its tile-local leader, reached by a walk
+// in the leader map: pixel -> run start -> ancestors -> leader.  The labels buffer holds the slots of border leaders until
 // this kernel overwrites it; a tile reads only its own slots, before writing.
 // Both lookup tables end in a sentinel entry (index TILE: map -> TILE, label
 // 0), which background and any out-of-range entry are clamped to.
@@ -1055,11 +1072,24 @@ __global__ void __launch_bounds__(NT, 8) k_number(const uint16_t* __restrict__ L
     const int r = warp + k * NWARPS;
     if (r >= t.th) continue;
     int out[PX];
+    uint32_t prev = 0xFFFFFFFFu;   // the run start of the pixel before
 #pragma unroll
     for (int j = 0; j < PX; ++j) {
-      // pixel -> run start -> leader
+      // pixel -> run start -> ... -> leader: the map's entries point ever
+      // lower until a leader, whose entry is itself (sentinel: TILE).  The
+      // pixels of a run share the walk: it is made once per run start.
       const uint32_t l = min((lw[k][j >> 1] >> (16 * (j & 1))) & 0xFFFFu, (uint32_t)TILE);
-      out[j] = lab[min((uint32_t)lmap[l], (uint32_t)TILE)];
+      if (l == prev) {
+        out[j] = out[j > 0 ? j - 1 : 0];
+      } else {
+        uint32_t x = l, y = min((uint32_t)lmap[x], (uint32_t)TILE);
+        for (int s = 0; s < TILE && y != x; ++s) {
+          x = y;
+          y = min((uint32_t)lmap[x], (uint32_t)TILE);
+        }
+        out[j] = lab[x];
+        prev = l;
+      }
     }
     int32_t* orow = Pi + (long long)(t.y0 + r) * g.W + t.x0 + xl;
     if (vec) {
