@@ -23,6 +23,7 @@ constexpr int MAX_DEVICES = 64;
 std::mutex g_mutex;
 int* g_status[MAX_DEVICES] = {nullptr};
 cudaMemPool_t g_pool[MAX_DEVICES] = {nullptr};
+cudaStream_t g_copy[MAX_DEVICES] = {nullptr};   // the host entry point's copy stream
 long long g_walk_cap = 0;   // 0: default
 std::atomic<long long> g_launches{0};
 
@@ -135,6 +136,20 @@ int validate(const void* img, int batch, int H, int W, int pb, int conn, int mod
   return CCL_OK;
 }
 
+// the current device's copy stream (created once, non-blocking)
+int device_copy_stream(cudaStream_t* out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) return CCL_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mutex);
+  if (!g_copy[dev]) {
+    cudaStream_t s;
+    if (cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking) != cudaSuccess) return CCL_ERR_CUDA;
+    g_copy[dev] = s;
+  }
+  *out = g_copy[dev];
+  return CCL_OK;
+}
+
 int device_status_ptr(int** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) return CCL_ERR_CUDA;
@@ -200,9 +215,9 @@ int device_pool(cudaMemPool_t* out) {
   } while (0)
 
 void k_tile_local_dispatch(int pb, int conn, int mode, const void* img, uint16_t* L16, int32_t* P,
-                           uint32_t* bm, uint32_t* cnt, const Border& bd, const Layout& L,
-                           const Geom& g, int cap, int* status, cudaStream_t st) {
-  CCL_DISPATCH(k_tile_local, L.nTiles, NT, L16, P, bm, cnt, bd, g, cap, status);
+                           uint32_t* bm, uint32_t* cnt, const Border& bd, long long tile0,
+                           long long ntiles, const Geom& g, int cap, int* status, cudaStream_t st) {
+  CCL_DISPATCH(k_tile_local, ntiles, NT, L16, P, bm, cnt, bd, g, cap, status, tile0);
 }
 
 void k_seams_dispatch(int pb, int conn, int mode, const void* img, const uint16_t* L16, int32_t* P,
@@ -212,63 +227,205 @@ void k_seams_dispatch(int pb, int conn, int mode, const void* img, const uint16_
                L.nTiles, cap, status);
 }
 
-// The whole labelling pipeline on `st`: `ws` is the workspace (layout L),
-// `status` the device word the kernels flag limits in, `events` whether the
-// optional per-stage events may be recorded.
-int run_pipeline(const void* img, int batch, int H, int W, int pb, int conn, int mode,
-                 uint32_t bgval, int32_t* labels, int32_t* n_out, const Layout& L, void* ws,
-                 int* status, bool events, cudaStream_t st) {
-  char* base = (char*)ws;
-  uint16_t* L16 = (uint16_t*)(base + L.offL16);
-  uint32_t* bm = (uint32_t*)(base + L.offBm);
-  uint32_t* cnt = (uint32_t*)(base + L.offCnt);
-  uint32_t* bsum = (uint32_t*)(base + L.offBsum);
+// The pipeline's pieces on `st`: `ws` is the workspace (layout L), `status`
+// the device word the kernels flag limits in.
+struct Pipe {
+  const void* img;
+  int batch, H, W, pb, conn, mode;
+  int32_t* labels;
+  int32_t* n_out;
+  const Layout* L;
+  uint16_t* L16;
+  uint32_t *bm, *cnt, *bsum;
   Border bd;
-  bd.rec = (uint32_t*)(base + L.offRec);
-  bd.list = (uint16_t*)(base + L.offList);
-  bd.cnt = (uint32_t*)(base + L.offBcnt);
+  Geom g;
+  int capTile, capImg;
+  int* status;
+  cudaStream_t st;
+};
+
+Pipe make_pipe(const void* img, int batch, int H, int W, int pb, int conn, int mode, uint32_t bgval,
+               int32_t* labels, int32_t* n_out, const Layout& L, void* ws, int* status,
+               cudaStream_t st) {
+  Pipe q;
+  q.img = img;
+  q.batch = batch;
+  q.H = H;
+  q.W = W;
+  q.pb = pb;
+  q.conn = conn;
+  q.mode = mode;
+  q.labels = labels;
+  q.n_out = n_out;
+  q.L = &L;
+  char* base = (char*)ws;
+  q.L16 = (uint16_t*)(base + L.offL16);
+  q.bm = (uint32_t*)(base + L.offBm);
+  q.cnt = (uint32_t*)(base + L.offCnt);
+  q.bsum = (uint32_t*)(base + L.offBsum);
+  q.bd.rec = (uint32_t*)(base + L.offRec);
+  q.bd.list = (uint16_t*)(base + L.offList);
+  q.bd.cnt = (uint32_t*)(base + L.offBcnt);
   long long capT = TILE + 1, capI = L.g.HW + 1;
   const long long user = g_walk_cap;
   if (user > 0) {
     capT = capT < user ? capT : user;
     capI = capI < user ? capI : user;
   }
-  const int capTile = (int)capT;
-  const int capImg = (int)(capI > INT32_MAX ? INT32_MAX : capI);
+  q.capTile = (int)capT;
+  q.capImg = (int)(capI > INT32_MAX ? INT32_MAX : capI);
+  // vector access when every row start keeps the needed alignment
+  q.g = L.g;
+  q.g.bgval = bgval;
+  const uintptr_t ia = (uintptr_t)img;
+  if (pb == 1) q.g.vec_img = (W % 8 == 0) && (ia % 8 == 0);
+  else if (pb == 2) q.g.vec_img = (W % 8 == 0) && (ia % 16 == 0);
+  else if (pb == 3) q.g.vec_img = (W % 8 == 0) && (ia % 8 == 0);   // 24-byte lanes on 8-byte boundaries
+  else q.g.vec_img = (W % 4 == 0) && (ia % 16 == 0);
+  q.g.vec_out = (W % 8 == 0) && ((uintptr_t)labels % 16 == 0);
+  q.status = status;
+  q.st = st;
+  return q;
+}
+
+// Start + Connect + Collapse for tiles [tile0, tile0 + ntiles)
+void launch_tile_local(const Pipe& q, long long tile0, long long ntiles) {
+  k_tile_local_dispatch(q.pb, q.conn, q.mode, q.img, q.L16, q.labels, q.bm, q.cnt, q.bd, tile0, ntiles,
+                        q.g, q.capTile, q.status, q.st);
+}
+void launch_seams(const Pipe& q) {
+  k_seams_dispatch(q.pb, q.conn, q.mode, q.img, q.L16, q.labels, q.bm, q.cnt, q.bd, *q.L, q.g, q.capImg,
+                   q.status, q.st);
+}
+void launch_scan(const Pipe& q) {
+  const Layout& L = *q.L;
+  k_scan_reduce<<<L.nScanBlocks, NT, 0, q.st>>>(q.cnt, L.nChunks, q.bsum);
+  k_scan_top<<<1, NT, 0, q.st>>>(q.bsum, L.nScanBlocks);
+  k_scan_down<<<L.nScanBlocks, NT, 0, q.st>>>(q.cnt, L.nChunks, q.bsum);
+  if (q.n_out)
+    k_region_counts<<<(q.batch + 255) / 256, 256, 0, q.st>>>(q.cnt, (long long)q.H * L.g.CPR, q.batch,
+                                                             q.n_out);
+}
+void launch_resolve(const Pipe& q) {
+  const Layout& L = *q.L;
+  k_resolve<<<(unsigned)((L.nTiles + RESOLVE_WARPS - 1) / RESOLVE_WARPS), 32 * RESOLVE_WARPS, 0, q.st>>>(
+      q.bd, L.nTiles, q.labels, q.bm, q.cnt, q.g, q.capImg, q.status);
+}
+// Number for tiles [tile0, tile0 + ntiles)
+void launch_number(const Pipe& q, long long tile0, long long ntiles) {
+  k_number<<<(unsigned)ntiles, NT, 0, q.st>>>(q.L16, q.labels, q.bm, q.cnt, q.bd, q.g, q.status, tile0);
+}
+
+// The whole labelling pipeline on `st`; `events` whether the optional
+// per-stage events may be recorded.
+int run_pipeline(const void* img, int batch, int H, int W, int pb, int conn, int mode,
+                 uint32_t bgval, int32_t* labels, int32_t* n_out, const Layout& L, void* ws,
+                 int* status, bool events, cudaStream_t st) {
+  const Pipe q = make_pipe(img, batch, H, W, pb, conn, mode, bgval, labels, n_out, L, ws, status, st);
   EventSet es;
   const bool timed = events && take_event_set(&es);
   auto mark = [&](int k) {
     if (timed) cudaEventRecord(es.ev[k], st);
   };
-  // vector access when every row start keeps the needed alignment
-  Geom g = L.g;
-  g.bgval = bgval;
-  const uintptr_t ia = (uintptr_t)img;
-  if (pb == 1) g.vec_img = (W % 8 == 0) && (ia % 8 == 0);
-  else if (pb == 2) g.vec_img = (W % 8 == 0) && (ia % 16 == 0);
-  else if (pb == 3) g.vec_img = (W % 8 == 0) && (ia % 8 == 0);   // 24-byte lanes on 8-byte boundaries
-  else g.vec_img = (W % 4 == 0) && (ia % 16 == 0);
-  g.vec_out = (W % 8 == 0) && ((uintptr_t)labels % 16 == 0);
-  const unsigned grid = (unsigned)L.nTiles;
   mark(0);
-  k_tile_local_dispatch(pb, conn, mode, img, L16, labels, bm, cnt, bd, L, g, capTile, status, st);
+  launch_tile_local(q, 0, L.nTiles);
   mark(1);
-  k_seams_dispatch(pb, conn, mode, img, L16, labels, bm, cnt, bd, L, g, capImg, status, st);
+  launch_seams(q);
   mark(2);
-  k_scan_reduce<<<L.nScanBlocks, NT, 0, st>>>(cnt, L.nChunks, bsum);
-  k_scan_top<<<1, NT, 0, st>>>(bsum, L.nScanBlocks);
-  k_scan_down<<<L.nScanBlocks, NT, 0, st>>>(cnt, L.nChunks, bsum);
-  if (n_out)
-    k_region_counts<<<(batch + 255) / 256, 256, 0, st>>>(cnt, (long long)H * L.g.CPR, batch, n_out);
+  launch_scan(q);
   mark(3);
-  k_resolve<<<(unsigned)((L.nTiles + RESOLVE_WARPS - 1) / RESOLVE_WARPS), 32 * RESOLVE_WARPS, 0, st>>>(bd, L.nTiles, labels, bm, cnt,
-                                                                          g, capImg, status);
+  launch_resolve(q);
   mark(4);
-  k_number<<<grid, NT, 0, st>>>(L16, labels, bm, cnt, bd, g, status);
+  launch_number(q, 0, L.nTiles);
   mark(5);
   if (timed) keep_event_set(es);
   g_launches += n_out ? 8 : 7;
   return cudaPeekAtLastError() == cudaSuccess ? CCL_OK : CCL_ERR_CUDA;
+}
+
+// The host entry point's pipeline.  The image goes up and the labels come
+// down in HOST_BANDS bands of whole tile rows on a copy stream `cs`: Start,
+// Connect and Collapse of a band run while the next band is copied in, and a
+// band's labels are copied out as soon as Number has written them (Number of
+// a tile reads and writes only that tile's part of the labels).  Seams, scan
+// and resolve need the whole image and run in between.
+constexpr int HOST_BANDS = 8;
+
+int run_host_banded(const void* img_host, int batch, int H, int W, int pb, int conn, int mode,
+                    int32_t* labels_host, int32_t* n_host, void* dImg, int32_t* dLab, int32_t* dN,
+                    const Layout& L, void* ws, int* status, cudaStream_t st, cudaStream_t cs) {
+  const Pipe q = make_pipe(dImg, batch, H, W, pb, conn, mode, 0u, dLab, dN, L, ws, status, st);
+  const long long tilesY = L.g.tilesY, tilesX = L.g.tilesX;
+  const long long tileRows = (long long)batch * tilesY;
+  const int K = (int)(tileRows < HOST_BANDS ? tileRows : HOST_BANDS);
+  cudaEvent_t ev[2 * HOST_BANDS + 2];
+  int made = 0;
+  int rc = CCL_OK;
+  for (; made < 2 * K + 2; ++made)
+    if (cudaEventCreateWithFlags(&ev[made], cudaEventDisableTiming) != cudaSuccess) {
+      rc = CCL_ERR_CUDA;
+      break;
+    }
+  // image rows (counted across the batch) of tile row tr: [first, end)
+  auto firstRow = [&](long long tr) {
+    const long long b = tr / tilesY, ty = tr - b * tilesY;
+    return b * H + ty * TH;
+  };
+  auto endRow = [&](long long tr) {
+    const long long b = tr / tilesY, ty = tr - b * tilesY;
+    return b * H + ((ty + 1) * TH < H ? (ty + 1) * TH : H);
+  };
+  auto bandRows = [&](int k, long long* tr0, long long* tr1) {
+    *tr0 = tileRows * k / K;
+    *tr1 = tileRows * (k + 1) / K;
+  };
+  if (rc == CCL_OK) {
+    const size_t rowBytes = (size_t)W * pb;
+    // the copy stream touches the buffers only after their allocation
+    cudaEventRecord(ev[2 * K], st);
+    cudaStreamWaitEvent(cs, ev[2 * K], 0);
+    for (int k = 0; k < K && rc == CCL_OK; ++k) {
+      long long tr0, tr1;
+      bandRows(k, &tr0, &tr1);
+      const long long r0 = firstRow(tr0), r1 = endRow(tr1 - 1);
+      if (cudaMemcpyAsync((char*)dImg + r0 * rowBytes, (const char*)img_host + r0 * rowBytes,
+                          (size_t)(r1 - r0) * rowBytes, cudaMemcpyHostToDevice, cs) != cudaSuccess ||
+          cudaEventRecord(ev[k], cs) != cudaSuccess)
+        rc = CCL_ERR_CUDA;
+    }
+    for (int k = 0; k < K && rc == CCL_OK; ++k) {
+      long long tr0, tr1;
+      bandRows(k, &tr0, &tr1);
+      cudaStreamWaitEvent(st, ev[k], 0);
+      launch_tile_local(q, tr0 * tilesX, (tr1 - tr0) * tilesX);
+    }
+    if (rc == CCL_OK) {
+      launch_seams(q);
+      launch_scan(q);
+      launch_resolve(q);
+    }
+    for (int k = 0; k < K && rc == CCL_OK; ++k) {
+      long long tr0, tr1;
+      bandRows(k, &tr0, &tr1);
+      launch_number(q, tr0 * tilesX, (tr1 - tr0) * tilesX);
+      const long long r0 = firstRow(tr0), r1 = endRow(tr1 - 1);
+      if (cudaEventRecord(ev[K + k], st) != cudaSuccess || cudaStreamWaitEvent(cs, ev[K + k], 0) != cudaSuccess ||
+          cudaMemcpyAsync(labels_host + r0 * W, dLab + r0 * W, (size_t)(r1 - r0) * W * sizeof(int32_t),
+                          cudaMemcpyDeviceToHost, cs) != cudaSuccess)
+        rc = CCL_ERR_CUDA;
+    }
+    if (rc == CCL_OK && n_host &&
+        cudaMemcpyAsync(n_host, dN, (size_t)batch * sizeof(int32_t), cudaMemcpyDeviceToHost, cs) !=
+            cudaSuccess)
+      rc = CCL_ERR_CUDA;
+    // the buffers are freed on `st` after the last copy
+    cudaEventRecord(ev[2 * K + 1], cs);
+    cudaStreamWaitEvent(st, ev[2 * K + 1], 0);
+    g_launches += 2 * K + 6;   // K tile_local, seams, 3 scans, region counts, resolve, K number
+  }
+  for (int i = 0; i < made; ++i) cudaEventDestroy(ev[i]);
+  if (rc == CCL_OK && cudaPeekAtLastError() != cudaSuccess) rc = CCL_ERR_CUDA;
+  return rc;
 }
 
 int run(const void* img, int batch, int H, int W, int pb, int conn, int mode, int32_t* labels,
@@ -474,17 +631,13 @@ int ccl_label_host(const void* img_host, int batch, int H, int W, int pixel_byte
   int32_t* dLab = (int32_t*)(buf + imgBytes);
   int32_t* dN = (int32_t*)(buf + imgBytes + labBytes);
   void* ws = buf + imgBytes + labBytes + nBytes;
-  if (cudaMemcpyAsync(dImg, img_host, npx * pixel_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
-    rc = CCL_ERR_CUDA;
+  int* status = nullptr;
+  cudaStream_t cs = nullptr;
+  rc = device_status_ptr(&status);
+  if (rc == CCL_OK) rc = device_copy_stream(&cs);
   if (rc == CCL_OK)
-    rc = run(dImg, batch, H, W, pixel_bytes, connectivity, mode, dLab, dN, L, ws, st);
-  if (rc == CCL_OK &&
-      cudaMemcpyAsync(labels_host, dLab, npx * 4, cudaMemcpyDeviceToHost, st) != cudaSuccess)
-    rc = CCL_ERR_CUDA;
-  if (rc == CCL_OK && n_regions_host &&
-      cudaMemcpyAsync(n_regions_host, dN, (size_t)batch * 4, cudaMemcpyDeviceToHost, st) !=
-          cudaSuccess)
-    rc = CCL_ERR_CUDA;
+    rc = run_host_banded(img_host, batch, H, W, pixel_bytes, connectivity, mode, labels_host,
+                         n_regions_host, dImg, dLab, dN, L, ws, status, st, cs);
   cudaFreeAsync(buf, st);
   const int sync = ccl_last_status(stream);
   return rc != CCL_OK ? rc : sync;

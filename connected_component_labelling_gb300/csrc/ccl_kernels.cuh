@@ -368,12 +368,13 @@ template <typename T, int CONN, bool BIN>
 __global__ void __launch_bounds__(NT, 8) k_tile_local(const T* __restrict__ img, uint16_t* __restrict__ L16,
                                                    int32_t* __restrict__ P, uint32_t* __restrict__ bm,
                                                    uint32_t* __restrict__ cnt, Border bd, Geom g,
-                                                   int cap, int* status) {
+                                                   int cap, int* status, long long tile0) {
   __shared__ int nborder;
   __shared__ __align__(16) int par[TILE];
   __shared__ __align__(16) uint8_t mark[TILE];
   __shared__ __align__(16) uint16_t jlist[NWARPS][TW];   // a row's joins, dealt out to the lanes
-  const TileCoord t = tile_coord(g);
+  const long long tile = tile0 + blockIdx.x;   // launches may cover a band of tiles
+  const TileCoord t = tile_coord_of(g, tile);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, xl = lane * PX;
   const long long ioff = (long long)t.b * g.HW;
   const T* im = img + ioff;
@@ -600,7 +601,7 @@ __global__ void __launch_bounds__(NT, 8) k_tile_local(const T* __restrict__ img,
   __syncthreads();
 
   // ---- border records: colour and leader of the left and right columns
-  uint32_t* rec = bd.rec + (long long)blockIdx.x * 4 * TH;
+  uint32_t* rec = bd.rec + tile * 4 * TH;
   if (threadIdx.x < 2 * t.th) {
     const int r = threadIdx.x % t.th, right = threadIdx.x / t.th;
     const int i = r * TW + (right ? t.tw - 1 : 0);
@@ -613,7 +614,7 @@ __global__ void __launch_bounds__(NT, 8) k_tile_local(const T* __restrict__ img,
 
   // ---- leaders whose region touches the border: a global parent slot and
   // an entry in the tile's border list
-  uint16_t* blist = bd.list + (long long)blockIdx.x * BLCAP;
+  uint16_t* blist = bd.list + tile * BLCAP;
 #pragma unroll
   for (int k = 0; k < RPW; ++k) {
     const int r = warp + k * NWARPS;
@@ -631,7 +632,7 @@ __global__ void __launch_bounds__(NT, 8) k_tile_local(const T* __restrict__ img,
     }
   }
   __syncthreads();
-  if (threadIdx.x == 0) bd.cnt[blockIdx.x] = (uint32_t)min(nborder, BLCAP);
+  if (threadIdx.x == 0) bd.cnt[tile] = (uint32_t)min(nborder, BLCAP);
 }
 
 // Connect across tile seams: the joins of the same rule as inside a tile,
@@ -986,10 +987,11 @@ __global__ void __launch_bounds__(32 * RESOLVE_WARPS, 32) k_resolve(Border bd, l
 __global__ void __launch_bounds__(NT, 8) k_number(const uint16_t* __restrict__ L16, int32_t* labels,
                                                const uint32_t* __restrict__ bm,
                                                const uint32_t* __restrict__ off, Border bd, Geom g,
-                                               int* status) {
+                                               int* status, long long tile0) {
   __shared__ __align__(16) int lab[TILE + 1];
   __shared__ __align__(16) uint16_t lmap[TILE + 8];   // the tile's leader map
-  const TileCoord t = tile_coord(g);
+  const long long tile = tile0 + blockIdx.x;   // launches may cover a band of tiles
+  const TileCoord t = tile_coord_of(g, tile);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, xl = lane * PX;
   const long long ioff = (long long)t.b * g.HW;
   const uint16_t* Li = L16 + ioff;
@@ -1006,7 +1008,6 @@ __global__ void __launch_bounds__(NT, 8) k_number(const uint16_t* __restrict__ L
   // leaders re-pointed across a seam (all in the tile's border list) carry the
   // label k_resolve stored, negated, in their slot: the list entry and then the
   // slot are loaded first, so that both loads overlap the rows' work below
-  const long long tile = blockIdx.x;
   const uint16_t* list = bd.list + tile * BLCAP;
   const int count = min((int)bd.cnt[tile], BLCAP);
   const int l0 = list[threadIdx.x];   // NT < BLCAP: always inside the tile's list
