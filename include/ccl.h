@@ -120,7 +120,10 @@ int ccl_label_ignore(const void* img, int batch, int H, int W,
  * ccl_label_host -- the whole call from host memory: copies `img_host` to
  * the device, labels it and copies the labels (and counts) back into
  * `labels_host` / `n_regions_host` (host pointers; page-locked memory is
- * fastest).  Device buffers come from the library's pool.  Returns after the
+ * fastest).  The copies run in bands of 16-row tile rows on a copy stream of
+ * the library's, overlapped with the kernels (a band is labelled inside its
+ * tiles while the next is copied in; a band's labels are copied out once
+ * numbered).  Device buffers come from the library's pool.  Returns after the
  * results are in host memory (the stream is synchronised); a tripped device
  * limit is returned directly as CCL_ERR_DEVICE_LIMIT.
  */

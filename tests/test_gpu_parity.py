@@ -172,6 +172,37 @@ def test_workspace_and_host_entry_points():
     assert int(hn[0]) == on
 
 
+@pytest.mark.parametrize("B,H,W,pb,conn,mode", [
+    (1, 20, 300, 1, 8, 1),      # 2 tile rows: fewer rows than copy bands
+    (5, 37, 257, 1, 4, 0),      # 15 tile rows in 8 bands that cross image boundaries
+    (3, 64, 520, 4, 8, 0),      # RGBA, whole tiles
+    (2, 45, 264, 3, 8, 1),      # 24-bit RGB
+])
+def test_host_entry_point_in_bands(B, H, W, pb, conn, mode):
+    """ccl_label_host copies the image up and the labels down in bands of
+    tile rows while the kernels run; results are those of the oracle."""
+    rng = np.random.default_rng(B * 1000 + H)
+    host = rng.integers(0, 3, size=(B, H, W, pb) if pb != 1 else (B, H, W)).astype(np.uint8)
+    olab, on = oracle.label(host, conn, mode)
+    himg = torch.from_numpy(host).contiguous().pin_memory()
+    hlab = torch.empty((B, H, W), dtype=torch.int32).pin_memory()
+    hn = torch.empty((B,), dtype=torch.int32)
+    with torch.cuda.device(DEV):
+        rc = ccl.ccl_label_host(himg.data_ptr(), B, H, W, pb, conn, mode, hlab.data_ptr(),
+                                hn.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    assert rc == ccl.CCL_OK
+    np.testing.assert_array_equal(hlab.numpy(), olab)
+    np.testing.assert_array_equal(hn.numpy(), on)
+    # pageable host memory and no region counts
+    plab = np.zeros((B, H, W), dtype=np.int32)
+    pimg = np.ascontiguousarray(host)
+    with torch.cuda.device(DEV):
+        rc = ccl.ccl_label_host(pimg.ctypes.data, B, H, W, pb, conn, mode, plab.ctypes.data, None,
+                                torch.cuda.current_stream().cuda_stream)
+    assert rc == ccl.CCL_OK
+    np.testing.assert_array_equal(plab, olab)
+
+
 def test_walk_cap_reports_device_limit_without_hanging():
     # a serpentine forces long union-find walks; a cap of 1 step must trip,
     # be reported, and leave the context usable
