@@ -222,30 +222,6 @@ __device__ __forceinline__ void load8<uint32_t>(const uint32_t* p, bool vec, int
   }
 }
 
-// shared-memory copies of a lane's 8 pixels (16-byte aligned addresses)
-template <typename T>
-__device__ __forceinline__ void st8s(T* s, const uint32_t c[PX]) {
-#pragma unroll
-  for (int j = 0; j < PX; ++j) s[j] = (T)c[j];
-}
-template <>
-__device__ __forceinline__ void st8s<uint32_t>(uint32_t* s, const uint32_t c[PX]) {
-  reinterpret_cast<uint4*>(s)[0] = make_uint4(c[0], c[1], c[2], c[3]);
-  reinterpret_cast<uint4*>(s)[1] = make_uint4(c[4], c[5], c[6], c[7]);
-}
-template <typename T>
-__device__ __forceinline__ void ld8s(const T* s, uint32_t c[PX]) {
-#pragma unroll
-  for (int j = 0; j < PX; ++j) c[j] = s[j];
-}
-template <>
-__device__ __forceinline__ void ld8s<uint32_t>(const uint32_t* s, uint32_t c[PX]) {
-  const uint4 a = reinterpret_cast<const uint4*>(s)[0];
-  const uint4 b = reinterpret_cast<const uint4*>(s)[1];
-  c[0] = a.x; c[1] = a.y; c[2] = a.z; c[3] = a.w;
-  c[4] = b.x; c[5] = b.y; c[6] = b.z; c[7] = b.w;
-}
-
 // ------------------------------------------------------------ shared memory
 // Union-find over tile-local indices r * TW + x.  Reads go through a
 // volatile pointer so every step sees other threads' links.
@@ -359,7 +335,8 @@ __device__ __forceinline__ int leader_of(const uint16_t* Li, int y, int x, const
 // ------------------------------------------------------------------ kernels
 
 // Occupancy matters more than a few spilled registers here: the in-tile
-// union-find is latency-bound, so the kernel is held to 32 registers (8
+// union-find (short, divergent walks in shared memory) runs best with every
+// warp slot of the SM filled, so the kernel is held to 32 registers (8
 // blocks of 256 threads per SM) and keeps no copy of the image in shared
 // memory: Start compares each row with the row above while both are in
 // registers (the row above was just loaded by a sibling warp: an L1 or L2
