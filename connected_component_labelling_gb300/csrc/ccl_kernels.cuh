@@ -595,17 +595,18 @@ __global__ void __launch_bounds__(NT, 8) k_tile_local(const T* __restrict__ img,
 #pragma unroll
   for (int k = 0; k < RPW; ++k) {
     const int r = warp + k * NWARPS;
-    unsigned m = rootm[k];
+    if (r >= t.th) continue;   // warp-uniform
+    // the marks of the lane's 8 pixels (bytes 0 or 1) as 8 bits
+    const uint2 mk = *reinterpret_cast<const uint2*>(mark + r * TW + xl);
+    unsigned m = rootm[k] & (((mk.x * 0x01020408u) >> 24) | (((mk.y * 0x01020408u) >> 24) << 4));
     while (m) {
       const int j = __ffs(m) - 1;
       m &= m - 1;
       const int i = r * TW + xl + j;
-      if (mark[i]) {
-        const int gi = (t.y0 + r) * g.W + t.x0 + xl + j;
-        Pi[gi] = gi;
-        const int slot = atomicAdd(&nborder, 1);
-        if (slot < BLCAP) blist[slot] = (uint16_t)i;
-      }
+      const int gi = (t.y0 + r) * g.W + t.x0 + xl + j;
+      Pi[gi] = gi;
+      const int slot = atomicAdd(&nborder, 1);
+      if (slot < BLCAP) blist[slot] = (uint16_t)i;
     }
   }
   __syncthreads();
