@@ -1058,8 +1058,11 @@ __global__ void __launch_bounds__(NT, 8) k_number(const uint16_t* __restrict__ L
       // lower until a leader, whose entry is itself (sentinel: TILE).  The
       // pixels of a run share the walk: it is made once per run start.
       const uint32_t l = min((lw[k][j >> 1] >> (16 * (j & 1))) & 0xFFFFu, (uint32_t)TILE);
-      if (l == prev) {
+      // the pixel before is in the same run: it has the same run start, or
+      // it is the run start (whose own entry is its leader or an ancestor)
+      if (l == prev || (j > 0 && l == (uint32_t)(r * TW + xl + j - 1))) {
         out[j] = out[j > 0 ? j - 1 : 0];
+        prev = l;
       } else {
         uint32_t x = l, y = min((uint32_t)lmap[x], (uint32_t)TILE);
         for (int s = 0; s < TILE && y != x; ++s) {
