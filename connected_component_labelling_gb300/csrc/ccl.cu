@@ -71,6 +71,17 @@ struct Layout {
   size_t offL16, offBm, offCnt, offBsum, offRec, offList, offBcnt, total;
 };
 
+// exact division by d (1 <= d < 2^31) for dividends below 2^31 (Granlund and
+// Montgomery, "Division by invariant integers using multiplication", 1994):
+// l = ceil(log2 d), magic = ceil(2^(32+l) / d), n / d = (n * magic) >> (32 + l).
+// The magic has at most 33 bits, so the product stays below 2^64.
+void magic_divisor(long long d, unsigned long long* magic, int* shift) {
+  int l = 0;
+  while ((1ll << l) < d) ++l;
+  *shift = 32 + l;
+  *magic = ((1ull << (32 + l)) + (unsigned long long)d - 1ull) / (unsigned long long)d;
+}
+
 int make_layout(int batch, int H, int W, Layout* L) {
   Geom& g = L->g;
   g.H = H;
@@ -86,12 +97,9 @@ int make_layout(int batch, int H, int W, Layout* L) {
   const long long nsb = (L->nChunks + SCAN_BLOCK - 1) / SCAN_BLOCK;
   if (nsb > (1ll << 30) || L->nTiles > (1ll << 31) - 1) return CCL_ERR_TOO_LARGE;
   L->nScanBlocks = (int)nsb;
-  // exact division by W for dividends below 2^31: l = ceil(log2 W),
-  // magic = ceil(2^(32+l) / W), d / W = (d * magic) >> (32 + l)
-  int l = 0;
-  while ((1ll << l) < W) ++l;
-  g.wshift = 32 + l;
-  g.wmagic = ((1ull << (32 + l)) + (unsigned long long)W - 1ull) / (unsigned long long)W;
+  magic_divisor(W, &g.wmagic, &g.wshift);
+  magic_divisor(g.tilesPerImage, &g.tmagic, &g.tshift);
+  magic_divisor(g.tilesX, &g.xmagic, &g.xshift);
   g.vec_img = 0;
   g.vec_out = 0;
   size_t o = 0;

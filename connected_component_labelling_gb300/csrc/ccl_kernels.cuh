@@ -85,6 +85,10 @@ struct Geom {
   long long tilesPerImage;
   unsigned long long wmagic;    // exact d / W for 0 <= d < 2^31: (d * wmagic) >> wshift
   int wshift;
+  unsigned long long tmagic;    // the same for d / tilesPerImage
+  int tshift;
+  unsigned long long xmagic;    // the same for d / tilesX
+  int xshift;
   int vec_img;                  // image rows allow 8-pixel vector loads
   int vec_out;                  // leader-map and label rows allow vector access
   uint32_t bgval;               // background value when background is ignored
@@ -107,11 +111,18 @@ struct TileCoord {
   int b, tx, y0, x0, th, tw;
 };
 
+// quotient of 0 <= d < 2^31 by the divisor whose magic pair is (m, sh)
+__device__ __forceinline__ int div_magic(int d, unsigned long long m, int sh) {
+  return (int)(((unsigned long long)(unsigned)d * m) >> sh);
+}
+
+// (tile indices are below 2^31: the host refuses larger grids)
 __device__ __forceinline__ TileCoord tile_coord_of(const Geom& g, long long tile) {
   TileCoord t;
-  t.b = (int)(tile / g.tilesPerImage);
-  const int rest = (int)(tile - (long long)t.b * g.tilesPerImage);
-  const int ty = rest / g.tilesX;
+  const int ti = (int)tile;
+  t.b = div_magic(ti, g.tmagic, g.tshift);
+  const int rest = ti - t.b * (int)g.tilesPerImage;
+  const int ty = div_magic(rest, g.xmagic, g.xshift);
   t.tx = rest - ty * g.tilesX;
   t.y0 = ty * TH;
   t.x0 = t.tx * TW;
@@ -122,9 +133,7 @@ __device__ __forceinline__ TileCoord tile_coord_of(const Geom& g, long long tile
 
 __device__ __forceinline__ TileCoord tile_coord(const Geom& g) { return tile_coord_of(g, blockIdx.x); }
 
-__device__ __forceinline__ int div_w(int d, const Geom& g) {
-  return (int)(((unsigned long long)(unsigned)d * g.wmagic) >> g.wshift);
-}
+__device__ __forceinline__ int div_w(int d, const Geom& g) { return div_magic(d, g.wmagic, g.wshift); }
 
 __device__ __forceinline__ void raise_flag(int* status, int f) { atomicOr(status, f); }
 
@@ -389,7 +398,9 @@ __global__ void __launch_bounds__(NT, 8) k_tile_local(const T* __restrict__ img,
         if (c[j] == g.bgval) fg &= ~(1u << j);
     }
     const uint32_t cl = __shfl_up_sync(FULL, c[PX - 1], 1);
-    const unsigned fgl = __shfl_up_sync(FULL, fg, 1);
+    // (all-pixels mode: the lane on the left is whole wherever this lane
+    // has a pixel, so its last pixel is foreground)
+    const unsigned fgl = BIN ? __shfl_up_sync(FULL, fg, 1) : 0x80u;
     unsigned eq = (lane > 0 && c[0] == cl) ? (fg & (fgl >> (PX - 1)) & 1u) : 0u;
 #pragma unroll
     for (int j = 1; j < PX; ++j) eq |= (c[j] == c[j - 1] ? 1u : 0u) << j;
@@ -580,7 +591,7 @@ __global__ void __launch_bounds__(NT, 8) k_tile_local(const T* __restrict__ img,
   // ---- border records: colour and leader of the left and right columns
   uint32_t* rec = bd.rec + tile * 4 * TH;
   if (threadIdx.x < 2 * t.th) {
-    const int r = threadIdx.x % t.th, right = threadIdx.x / t.th;
+    const int right = (int)threadIdx.x >= t.th, r = (int)threadIdx.x - right * t.th;
     const int i = r * TW + (right ? t.tw - 1 : 0);
     const int p = par[i];
     const int lead = p < 0 ? -1 : find_s(par, i, cap, status);
@@ -1221,7 +1232,7 @@ __global__ void __launch_bounds__(STATS_NT) k_region_stats(const int32_t* __rest
   const long long perImage = (long long)areasY * g.tilesX;
   const int b = (int)(blockIdx.x / perImage);
   const int rest = (int)(blockIdx.x - (long long)b * perImage);
-  const int ay = rest / g.tilesX, ax = rest - ay * g.tilesX;
+  const int ay = div_magic(rest, g.xmagic, g.xshift), ax = rest - ay * g.tilesX;
   const int y0 = ay * SR, y1 = min(y0 + SR, g.H) - 1;   // rows y0..y1
   const int x0 = ax * TW, x1 = min(x0 + TW, g.W) - 1;   // columns x0..x1
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, xl = lane * PX;
