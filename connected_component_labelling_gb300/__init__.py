@@ -189,11 +189,12 @@ def label_ignore(img, ignore_value, connectivity=8, out=None, n_out=None, worksp
     B, H, W, pb, squeeze = image_geometry(img)
     if out is None:
         out = torch.empty((B, H, W), dtype=torch.int32, device=img.device)
+    _check_tensor(out, "out", torch.int32, B * H * W, img.device)
     if n_out is None:
         n_out = torch.empty((B,), dtype=torch.int32, device=img.device)
+    _check_tensor(n_out, "n_out", torch.int32, B, img.device)
+    wp, wb = _workspace_arg(workspace, img.device)
     st = stream if stream is not None else torch.cuda.current_stream(img.device)
-    wp, wb = (workspace.data_ptr(), workspace.numel() * workspace.element_size()) \
-        if workspace is not None else (None, 0)
     with torch.cuda.device(img.device):
         rc = ccl_label_ignore(img.data_ptr(), B, H, W, pb, connectivity,
                               int(ignore_value) & 0xFFFFFFFF, out.data_ptr(), n_out.data_ptr(),
@@ -227,18 +228,27 @@ def region_stats(labels, n_regions, capacity=None, workspace=None, stream=None):
     import torch
     if not labels.is_cuda:
         raise ValueError("region_stats() needs CUDA tensors; the library has no CPU path")
+    if labels.dtype != torch.int32:
+        raise ValueError("labels must be int32, not %s" % labels.dtype)
     labels = labels.contiguous()
     if labels.dim() == 2:
         B, (H, W) = 1, labels.shape
-    else:
+    elif labels.dim() == 3:
         B, H, W = labels.shape
+    else:
+        raise ValueError("expected [B,]H,W labels")
+    if not isinstance(n_regions, torch.Tensor) or n_regions.device != labels.device:
+        raise ValueError("n_regions must be a tensor on the labels' device")
     n = n_regions.reshape(-1).to(torch.int32).contiguous()
+    if n.numel() != B:
+        raise ValueError("n_regions holds %d counts for %d images" % (n.numel(), B))
     if capacity is None:
         capacity = int(n.to(torch.int64).sum().item())
+    if capacity < 0:
+        raise ValueError("capacity must be >= 0")
     raw = torch.empty((max(capacity, 1) * STAT_BYTES,), dtype=torch.uint8, device=labels.device)
     st = stream if stream is not None else torch.cuda.current_stream(labels.device)
-    wp, wb = (workspace.data_ptr(), workspace.numel() * workspace.element_size()) \
-        if workspace is not None else (None, 0)
+    wp, wb = _workspace_arg(workspace, labels.device)
     with torch.cuda.device(labels.device):
         rc = ccl_region_stats(labels.data_ptr(), B, H, W, n.data_ptr(), raw.data_ptr(), capacity,
                               wp, wb, st.cuda_stream)
@@ -282,6 +292,30 @@ _MODES = {"all": CCL_MODE_ALL, "binary": CCL_MODE_BINARY,
           CCL_MODE_ALL: CCL_MODE_ALL, CCL_MODE_BINARY: CCL_MODE_BINARY}
 
 
+def _check_tensor(t, name, dtype, numel, device):
+    """Caller-supplied buffers go to the kernels as raw pointers: each must be a
+    contiguous tensor of the expected dtype and size on the image's device."""
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch.Tensor" % name)
+    if t.device != device:
+        raise ValueError("%s is on %s, the input on %s" % (name, t.device, device))
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError("%s must be %s, not %s" % (name, dtype, t.dtype))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if numel is not None and t.numel() != numel:
+        raise ValueError("%s holds %d elements, %d expected" % (name, t.numel(), numel))
+
+
+def _workspace_arg(workspace, device):
+    """(pointer, bytes) of an optional caller workspace on ``device``."""
+    if workspace is None:
+        return None, 0
+    _check_tensor(workspace, "workspace", None, None, device)
+    return workspace.data_ptr(), workspace.numel() * workspace.element_size()
+
+
 def image_geometry(img):
     """(batch, H, W, pixel_bytes, squeeze) of a [B,]H,W tensor of 1/2/4-byte
     pixels, or a [B,]H,W,C uint8 tensor whose C (2, 3 or 4) bytes form one
@@ -312,8 +346,11 @@ def label(img, connectivity=8, mode="all", out=None, n_out=None, workspace=None,
     m = _MODES[mode]
     if out is None:
         out = torch.empty((B, H, W), dtype=torch.int32, device=img.device)
+    _check_tensor(out, "out", torch.int32, B * H * W, img.device)
     if n_out is None:
         n_out = torch.empty((B,), dtype=torch.int32, device=img.device)
+    _check_tensor(n_out, "n_out", torch.int32, B, img.device)
+    wp, wb = _workspace_arg(workspace, img.device)
     st = stream if stream is not None else torch.cuda.current_stream(img.device)
     sp = st.cuda_stream
     with torch.cuda.device(img.device):
@@ -322,8 +359,7 @@ def label(img, connectivity=8, mode="all", out=None, n_out=None, workspace=None,
                            n_out.data_ptr(), sp)
         else:
             rc = ccl_label_ws(img.data_ptr(), B, H, W, pb, connectivity, m, out.data_ptr(),
-                              n_out.data_ptr(), workspace.data_ptr(),
-                              workspace.numel() * workspace.element_size(), sp)
+                              n_out.data_ptr(), wp, wb, sp)
     if rc != CCL_OK:
         raise CCLError(rc, "ccl_label")
     if squeeze:

@@ -564,8 +564,8 @@ __global__ void __launch_bounds__(NT, 8) k_tile_local(const T* __restrict__ img,
       // to k_number); any other pixel: its run start
       int e = pj[j];
       if (((starts >> j) & 1u) && e != i0 + j) e = par[e];
-      const uint32_t v = e < 0 ? (uint32_t)LBG : (uint32_t)e;
-      if (j & 1) lw[j >> 1] |= v << 16;
+      const uint32_t v = min((uint32_t)e, (uint32_t)LBG);   // background (-1) -> LBG
+      if (j & 1) lw[j >> 1] = __byte_perm(lw[j >> 1], v, 0x5410);
       else lw[j >> 1] = v;
     }
     rm &= vmask;

@@ -269,3 +269,37 @@ def test_ignore_zero_equals_binary_mode():
     b, nb = ccl.label(img, 8, "binary")
     ccl.check_status()
     assert torch.equal(a, b) and torch.equal(na, nb)
+
+
+def test_tensor_wrappers_reject_bad_buffers():
+    """Caller buffers reach the kernels as raw pointers, so the tensor
+    wrappers refuse a wrong dtype, size, layout or device before any call
+    into the library; the right buffers then label as usual."""
+    img = workloads.random_levels(40, 300, 3, seed=5).to(DEV)
+    n = img.numel()
+    bad_outs = [torch.empty(n, dtype=torch.int64, device=DEV),            # dtype
+                torch.empty(n - 1, dtype=torch.int32, device=DEV),        # size
+                torch.empty((300, 40), dtype=torch.int32, device=DEV).t(),  # layout
+                torch.empty(n, dtype=torch.int32)]                       # host memory
+    for out in bad_outs:
+        with pytest.raises(ValueError):
+            ccl.label(img, 8, "all", out=out)
+        with pytest.raises(ValueError):
+            ccl.label_ignore(img, 0, 8, out=out)
+    for n_out in (torch.empty(2, dtype=torch.int32, device=DEV), torch.empty(1, dtype=torch.int32)):
+        with pytest.raises(ValueError):
+            ccl.label(img, 8, "all", n_out=n_out)
+    with pytest.raises(ValueError):
+        ccl.label(img, 8, "all", workspace=torch.empty(1 << 20, dtype=torch.uint8))
+    lab, cnt = ccl.label(img, 8, "all", out=torch.empty(n, dtype=torch.int32, device=DEV),
+                         n_out=torch.empty(1, dtype=torch.int32, device=DEV))
+    ccl.check_status()
+    olab, on = oracle.label(to_np(img.cpu()), 8, oracle.MODE_ALL)
+    np.testing.assert_array_equal(lab.cpu().numpy().reshape(olab.shape), olab)
+    with pytest.raises(ValueError):
+        ccl.region_stats(lab.view(40, 300).to(torch.int64), cnt)
+    with pytest.raises(ValueError):
+        ccl.region_stats(lab.view(40, 300), cnt.cpu())
+    with pytest.raises(ValueError):
+        ccl.region_stats(lab.view(40, 300), torch.cat([cnt, cnt]))
+    ccl.check_status()
