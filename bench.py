@@ -36,6 +36,7 @@ if ROOT not in sys.path:
 METRIC = "Gpixel/s labelled (device-timed) and % of HBM roofline, 1 GB300"
 UNIT = "Gpixel/s"
 FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 8000.0          # the GB300's nominal HBM3e bandwidth, for the second fraction
 L2_BYTES = 129 * 1024 * 1024
 REF_ROWS = 1200           # rows of the sheet one reference step labels
 CPU_BASELINE_ROWS = 9600  # rows of the sheet the cpu_baseline leg labels
@@ -341,14 +342,18 @@ def main():
     launches0 = ccl.ccl_kernel_launches()
     t_wall0 = time.time()
     if not small:
+        # one event after each step as well, for the per-step median and minimum
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
+        marks = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
         e0.record(stream)
-        for _ in range(args.steps):
+        for k in range(args.steps):
             step()
+            marks[k].record(stream)
         e1.record(stream)
         torch.cuda.synchronize(dev)
         total_ms = e0.elapsed_time(e1)
+        step_ms = [(marks[k - 1] if k else e0).elapsed_time(marks[k]) for k in range(args.steps)]
     else:
         # inputs fit in L2: flush it between steps, outside the timed events
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -359,7 +364,8 @@ def main():
             step()
             b.record(stream)
         torch.cuda.synchronize(dev)
-        total_ms = sum(a.elapsed_time(b) for a, b in evs)
+        step_ms = [a.elapsed_time(b) for a, b in evs]
+        total_ms = sum(step_ms)
     t_wall1 = time.time()
     launches = ccl.ccl_kernel_launches() - launches0
     barrier(world)
@@ -402,7 +408,11 @@ def main():
     path_gbs = (pb + 4) * px / (ms * 1e-3) / 1e9
     roofline_path = {"bound": "hbm", "alg_bytes_per_px": pb + 4, "achieved": path_gbs,
                      "peak": peak, "unit": "GB/s", "frac": path_gbs / peak,
-                     "note": "whole ccl_label call: image read once + int32 label write"}
+                     "frac_of_nominal": path_gbs / NOMINAL_HBM_GBS,
+                     "nominal_peak": NOMINAL_HBM_GBS,
+                     "note": "whole ccl_label call: image read once + int32 label write; "
+                             "frac against the measured copy bandwidth, frac_of_nominal "
+                             "against the GB300's nominal 8 TB/s"}
 
     # ---- region statistics of the labels just made (the step after
     # labelling), timed on their own: labels read once, one 40-byte entry
@@ -516,6 +526,7 @@ def main():
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
+                "ms_per_step_median": statistics.median(step_ms), "ms_per_step_min": min(step_ms),
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                 "dtype": "int32", "data": "synthetic",
                 "config": dict(cfg, l2=("L2 flushed between steps (outside the events)" if small

@@ -301,5 +301,5 @@ def test_tensor_wrappers_reject_bad_buffers():
     with pytest.raises(ValueError):
         ccl.region_stats(lab.view(40, 300), cnt.cpu())
     with pytest.raises(ValueError):
-        ccl.region_stats(lab.view(40, 300), torch.cat([cnt, cnt]))
+        ccl.region_stats(lab.view(40, 300), cnt.reshape(1).repeat(2))
     ccl.check_status()
