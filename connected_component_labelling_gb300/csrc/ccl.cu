@@ -144,6 +144,17 @@ int validate(const void* img, int batch, int H, int W, int pb, int conn, int mod
   return CCL_OK;
 }
 
+// A caller's workspace must not share bytes with the image, the labels or
+// the counts: the kernels write all of it.
+bool workspace_overlaps(const void* ws, size_t wsBytes, const void* img, int batch, int H, int W,
+                        int pb, const int32_t* labels, const int32_t* n_out) {
+  const uintptr_t wa = (uintptr_t)ws, wb = wa + wsBytes;
+  const uintptr_t n = (uintptr_t)batch * (uintptr_t)H * (uintptr_t)W;
+  auto hit = [&](uintptr_t a, uintptr_t bytes) { return a < wb && wa < a + bytes; };
+  return hit((uintptr_t)img, n * (uintptr_t)pb) || hit((uintptr_t)labels, n * 4) ||
+         (n_out && hit((uintptr_t)n_out, (uintptr_t)batch * 4));
+}
+
 // the current device's copy stream (created once, non-blocking)
 int device_copy_stream(cudaStream_t* out) {
   int dev = 0;
@@ -540,6 +551,8 @@ int ccl_label_ws(const void* img, int batch, int H, int W, int pixel_bytes, int 
   if (rc != CCL_OK) return rc;
   if (!workspace || ((uintptr_t)workspace & 255)) return CCL_ERR_INVALID_ARG;
   if (workspace_bytes < L.total) return CCL_ERR_NO_MEMORY;
+  if (workspace_overlaps(workspace, L.total, img, batch, H, W, pixel_bytes, labels_i32, n_regions_out))
+    return CCL_ERR_INVALID_ARG;
   return run(img, batch, H, W, pixel_bytes, connectivity, mode, labels_i32, n_regions_out, L,
              workspace, st);
 }
@@ -584,6 +597,9 @@ int ccl_label_ignore(const void* img, int batch, int H, int W, int pixel_bytes, 
   if (workspace) {
     if ((uintptr_t)workspace & 255) return CCL_ERR_INVALID_ARG;
     if (workspace_bytes < L.total) return CCL_ERR_NO_MEMORY;
+    if (workspace_overlaps(workspace, L.total, img, batch, H, W, pixel_bytes, labels_i32,
+                           n_regions_out))
+      return CCL_ERR_INVALID_ARG;
     int* status = nullptr;
     rc = device_status_ptr(&status);
     if (rc != CCL_OK) return rc;

@@ -91,7 +91,9 @@ size_t ccl_workspace_bytes(int batch, int H, int W, int pixel_bytes,
  * ccl_label_ws -- ccl_label with caller-provided scratch: `workspace` is a
  * device pointer to at least ccl_workspace_bytes(...) bytes, 256-byte
  * aligned, owned by the caller and not used by any other call in flight.
- * Returns CCL_ERR_NO_MEMORY if workspace_bytes is too small.
+ * Returns CCL_ERR_NO_MEMORY if workspace_bytes is too small and
+ * CCL_ERR_INVALID_ARG if the workspace it uses shares bytes with the image,
+ * the labels or the counts.
  */
 int ccl_label_ws(const void* img, int batch, int H, int W, int pixel_bytes,
                  int connectivity, int mode, int32_t* labels_i32,

@@ -113,6 +113,19 @@ def test_workspace_checks_on_host(lib):
     assert ccl.ccl_label_ws(*args, FAKE * 128, need - 1, None) == ccl.CCL_ERR_NO_MEMORY
     assert ccl.ccl_label_ws(*args, FAKE * 128 + 16, need, None) == ccl.CCL_ERR_INVALID_ARG
     assert ccl.ccl_label_ws(*args, None, need, None) == ccl.CCL_ERR_INVALID_ARG
+    # a workspace sharing bytes with the image, the labels or the counts
+    img, labels, counts = FAKE * 64, FAKE * 128, FAKE * 192
+    base = (img, 1, 64, 64, 1, 8, 0, labels)
+    for ws in (img - (need // 256) * 256 + 256,    # its end reaches the image
+               img + 1024,                          # inside the image
+               labels + 4096 * 4 - 256):            # from the labels' last bytes on
+        ws -= ws % 256
+        assert ccl.ccl_label_ws(*base, None, ws, need, None) == ccl.CCL_ERR_INVALID_ARG, hex(ws)
+        assert ccl.ccl_label_ignore(*base[:6], 5, labels, None, ws, need, None) == \
+            ccl.CCL_ERR_INVALID_ARG, hex(ws)
+    assert need % 256 == 0
+    ws = counts + 256 - need                        # its last 256 bytes hold the counts
+    assert ccl.ccl_label_ws(*base, counts, ws, need, None) == ccl.CCL_ERR_INVALID_ARG
 
 
 def test_stage_names_and_counter(lib):
