@@ -232,6 +232,28 @@ def time_oracle(img_np, conn, mode):
     return time.perf_counter() - t0
 
 
+def host_info():
+    """The host the oracle is timed on: logical cores and the CPU model as
+    /proc/cpuinfo names it (x86: model name; Arm: implementer and part)."""
+    import platform
+    info = {"nproc": os.cpu_count(), "machine": platform.machine()}
+    try:
+        fields = {}
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if ":" in line:
+                    k, v = line.split(":", 1)
+                    fields.setdefault(k.strip(), v.strip())
+        if "model name" in fields:
+            info["cpu"] = fields["model name"]
+        elif "CPU part" in fields:
+            info["cpu"] = "implementer %s part %s" % (fields.get("CPU implementer", "?"),
+                                                      fields["CPU part"])
+    except OSError:
+        pass
+    return info
+
+
 def run_reference(args, world, rank):
     """The oracle as it stands, timed on this machine's host cores, one step =
     one labelling of a REF_ROWS-row band of the sheet."""
@@ -259,7 +281,7 @@ def run_reference(args, world, rank):
                        "W": 33600, "pixel_bytes": 4, "connectivity": 8, "mode": "all",
                        "sample_rows": rows},
             "cpu_baseline": {"value": gpxs, "unit": UNIT, "cores": 1, "kind": "oracle",
-                             "sample": sample},
+                             "sample": sample, "host": host_info()},
             "e2e": {"value": gpxs, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -521,7 +543,8 @@ def main():
         band_px = band.size // 3 if pb == 3 else band.size
         cpu_baseline = {"value": band_px / dt / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
                         "sample": "rows 0-%d of the sheet (%d px), one single-threaded BFS pass, "
-                                  "%.1f s" % (CPU_BASELINE_ROWS, band_px, dt)}
+                                  "%.1f s" % (CPU_BASELINE_ROWS, band_px, dt),
+                        "host": host_info()}
 
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,

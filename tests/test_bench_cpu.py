@@ -38,6 +38,7 @@ def test_reference_arm_line():
     assert KEYS <= set(d)
     assert d["impl"] == "reference" and d["unit"] == "Gpixel/s" and d["value"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] == 1
+    assert d["cpu_baseline"]["host"]["nproc"] >= 1
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["config"]["sample_rows"] == 32
     assert d["config"]["workload"] == "c4_sheet_24000x33600_rgba"
 
