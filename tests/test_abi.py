@@ -179,3 +179,20 @@ def test_counters_only_in_the_counters_build(lib):
     # the product library has no counters compiled in
     assert ccl.ccl_debug_counters(buf, 8, 0) == ccl.CCL_ERR_INVALID_ARG
     assert len(ccl.COUNTER_NAMES) == 8
+
+
+def test_plain_c_consumer_links_and_runs(lib, tmp_path):
+    """The header is C: a C99 program (tests/c/abi_consumer.c) compiles against
+    it with -pedantic, links against libccl.so and checks the entry points
+    that answer on the host, the statistics struct layout included."""
+    import subprocess
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    so = ccl.build()
+    exe = str(tmp_path / "abi_consumer")
+    subprocess.check_call(["gcc", "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror",
+                           "-I", os.path.join(root, "include"),
+                           os.path.join(root, "tests", "c", "abi_consumer.c"),
+                           "-o", exe, so, "-Wl,-rpath," + os.path.dirname(so)])
+    out = subprocess.run([exe], capture_output=True, text=True, timeout=120)
+    assert out.returncode == 0, (out.returncode, out.stdout, out.stderr)
+    assert "C consumer ok" in out.stdout
