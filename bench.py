@@ -110,12 +110,17 @@ def load_peaks():
 
 
 def source_sha():
-    """Hash of the CUDA sources: a committed ncu traffic figure is only used
-    while the kernels it was measured on are unchanged."""
+    """Hash of the CUDA sources without their comments and whitespace: a
+    committed ncu traffic figure is only used while the code it was measured
+    on is unchanged (a comment edit does not change a kernel)."""
+    import re
     h = hashlib.sha256()
     for name in ("ccl.cu", "ccl_kernels.cuh"):
-        with open(os.path.join(ROOT, "connected_component_labelling_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "connected_component_labelling_gb300", "csrc", name)) as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)   # block comments
+        text = re.sub(r"//[^\n]*", " ", text)                 # line comments
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 

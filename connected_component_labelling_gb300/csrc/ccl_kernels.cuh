@@ -5,16 +5,17 @@
 //
 //   k_tile_local  Start + Connect + Collapse inside one tile, in shared
 //                 memory.  A lane owns 8 consecutive pixels of a row; runs of
-//                 equal colour are found with a warp scan of run starts
-//                 (ch. 08 switch 1, the warp finds the runs) so that a run is
-//                 one union-find node.  Joins go to the row above first and
+//                 equal colour are found from equal-to-left bit masks and one
+//                 warp vote for the last run start left of each lane (ch. 08
+//                 switch 1, the warp finds the runs), so that a run is one
+//                 union-find node.  Joins go to the row above first and
 //                 skip what the left neighbour already joins (ch. 08 "First,
 //                 the order of the joins" and switch 2, the Wu-Otoo-Suzuki
 //                 scan mask); walks halve paths with the same atomic minimum
 //                 (switch 3).  Output: a 2-byte leader map (a pixel's run
 //                 start; for a run start, its tile-local leader in the
-//                 tile's first and last rows and column 0, elsewhere an
-//                 ancestor on the way to it),
+//                 tile's first and last rows, column 0 and the run holding
+//                 the last column, elsewhere an ancestor on the way to it),
 //                 a leader bitmap, a leader count per 256-pixel chunk of a
 //                 row, and a global parent slot (its own raster index) for
 //                 every leader whose region touches the tile border.
