@@ -86,10 +86,11 @@ int make_layout(int batch, int H, int W, Layout* L) {
   Geom& g = L->g;
   g.H = H;
   g.W = W;
-  g.tilesX = (W + TW - 1) / TW;
-  g.tilesY = (H + TH - 1) / TH;
-  g.WPR = (W + 31) / 32;
-  g.CPR = (W + CHUNK - 1) / CHUNK;
+  // (in 64 bits: W or H may be as large as 2^31 - 1)
+  g.tilesX = (int)(((long long)W + TW - 1) / TW);
+  g.tilesY = (int)(((long long)H + TH - 1) / TH);
+  g.WPR = (int)(((long long)W + 31) / 32);
+  g.CPR = (int)(((long long)W + CHUNK - 1) / CHUNK);
   g.HW = (long long)H * W;
   g.tilesPerImage = (long long)g.tilesX * g.tilesY;
   L->nTiles = g.tilesPerImage * batch;
@@ -750,7 +751,7 @@ int ccl_region_stats(const int32_t* labels_i32, int batch, int H, int W, const i
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     sms = 1;
   k_stats_init<<<(unsigned)(sms * 8), NT, 0, st>>>(stats, (long long)capacity, off, batch, status);
-  const long long areas = (long long)batch * ((H + SR - 1) / SR) * L.g.tilesX;
+  const long long areas = (long long)batch * (((long long)H + SR - 1) / SR) * L.g.tilesX;
   k_region_stats<<<(unsigned)areas, STATS_NT, 0, st>>>(labels_i32, n_regions, off, stats,
                                                  (long long)capacity, g, status);
   g_launches += 3;

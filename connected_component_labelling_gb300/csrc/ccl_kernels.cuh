@@ -1229,13 +1229,13 @@ __global__ void __launch_bounds__(STATS_NT) k_region_stats(const int32_t* __rest
   }
   __syncthreads();
   // block -> image, area row, area column
-  const int areasY = (g.H + SR - 1) / SR;
+  const int areasY = (int)(((long long)g.H + SR - 1) / SR);
   const long long perImage = (long long)areasY * g.tilesX;
   const int b = (int)(blockIdx.x / perImage);
   const int rest = (int)(blockIdx.x - (long long)b * perImage);
   const int ay = div_magic(rest, g.xmagic, g.xshift), ax = rest - ay * g.tilesX;
-  const int y0 = ay * SR, y1 = min(y0 + SR, g.H) - 1;   // rows y0..y1
-  const int x0 = ax * TW, x1 = min(x0 + TW, g.W) - 1;   // columns x0..x1
+  const int y0 = ay * SR, y1 = y0 + min(SR, g.H - y0) - 1;   // rows y0..y1
+  const int x0 = ax * TW, x1 = x0 + min(TW, g.W - x0) - 1;   // columns x0..x1
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, xl = lane * PX;
   const int nb = n_regions[b];
   const long long base = off[b];

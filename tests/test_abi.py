@@ -196,3 +196,18 @@ def test_plain_c_consumer_links_and_runs(lib, tmp_path):
     out = subprocess.run([exe], capture_output=True, text=True, timeout=120)
     assert out.returncode == 0, (out.returncode, out.stdout, out.stderr)
     assert "C consumer ok" in out.stdout
+
+
+def test_workspace_bytes_of_the_largest_shapes(lib):
+    """Geometry near 2^31 is computed in 64 bits: the one-row image of
+    2^31 - 1 pixels needs about 7.4 B/px (the per-tile border lists of its
+    8.4 M one-row tiles), the square just below 2^31 pixels about 2.5 B/px,
+    and 2^31 pixels are refused."""
+    w1 = (1 << 31) - 1
+    row = ccl.ccl_workspace_bytes(1, 1, w1, 1, 8, 0)
+    assert 0 < row < 8 * w1
+    sq = ccl.ccl_workspace_bytes(1, 46340, 46340, 1, 8, 0)
+    assert 2 * 46340 ** 2 < sq < 3 * 46340 ** 2
+    col = ccl.ccl_workspace_bytes(1, w1, 1, 1, 8, 0)
+    assert col > 0
+    assert ccl.ccl_workspace_bytes(1, 1 << 16, 1 << 15, 1, 8, 0) == 0
