@@ -410,8 +410,11 @@ def main():
     peak, peak_kind = load_peaks()
     names = [ccl.ccl_stage_name(k) for k in range(len(stage_ms))]
     per_call = [s / max(1, ncalls) for s in stage_ms]
-    # algorithmic bytes per pixel of each stage that streams the image
-    alg = {"tile_local": pb + 4, "number": 4 + 4}
+    # bytes per pixel charged to the stages that stream whole images:
+    # tile_local carries the method's figure (image read once + int32 labels
+    # written), the per-unit figure of the roofline when it dominates; number
+    # its own least traffic (leader map read, 2 B, + labels written, 4 B)
+    alg = {"tile_local": pb + 4, "number": 2 + 4}
     dom = max(range(len(per_call)), key=lambda k: per_call[k]) if per_call else 0
     dom_name = names[dom] if names else "tile_local"
     dom_alg = alg.get(dom_name)
