@@ -74,8 +74,8 @@ enum { CCL_MODE_ALL = 0, CCL_MODE_BINARY = 1 };
  *   labels_i32     device pointer, batch*H*W int32, written completely
  *   n_regions_out  device pointer to batch int32 (region count per image),
  *                  or NULL
- * Scratch (about H*W/256*4 + H*ceil(W/32)*4 bytes per image) comes from a
- * stream-ordered memory pool the library keeps per device.
+ * Scratch (ccl_workspace_bytes(...) bytes, about 2.5 bytes per pixel) comes
+ * from a stream-ordered memory pool the library keeps per device.
  * Returns CCL_OK or an error status; nothing is written on an argument error.
  */
 int ccl_label(const void* img, int batch, int H, int W, int pixel_bytes,
