@@ -163,6 +163,26 @@ def test_rgba_alpha_counts():
     assert n == 2 and lab[1, 1] == 2
 
 
+@pytest.mark.parametrize("conn", [4, 8])
+def test_rgb_three_byte_pixels(conn):
+    """Packed 24-bit RGB ("every-colour", ch. 08 "Tried and dropped": RGB read
+    as is): labelling the [H, W, 3] bytes gives the labels of the same colours
+    packed into one 32-bit word with an opaque alpha, and two pixels that
+    differ only in their third byte are different colours."""
+    rng = np.random.default_rng(11)
+    rgb = rng.integers(0, 2, size=(37, 53, 3)).astype(np.uint8) * np.array([0, 7, 200], np.uint8)
+    packed = (rgb[..., 0].astype(np.uint32) | (rgb[..., 1].astype(np.uint32) << 8)
+              | (rgb[..., 2].astype(np.uint32) << 16) | np.uint32(0xFF000000))
+    lab3, n3 = oracle.label(rgb[None], conn, oracle.MODE_ALL)
+    lab4, n4 = oracle.label(packed, conn, oracle.MODE_ALL)
+    np.testing.assert_array_equal(lab3[0], lab4)
+    assert n3[0] == n4
+    two = np.zeros((1, 1, 2, 3), np.uint8)
+    two[0, 0, 1, 2] = 1                               # only the blue byte differs
+    lab, n = oracle.label(two, conn, oracle.MODE_ALL)
+    assert n[0] == 2 and lab[0, 0].tolist() == [1, 2]
+
+
 def test_empty_and_degenerate_shapes():
     for shape in [(0, 5), (5, 0), (0, 0)]:
         lab, n = oracle.label(np.zeros(shape, np.uint8), 8, oracle.MODE_ALL)
