@@ -115,8 +115,11 @@ def source_sha():
     on is unchanged (a comment edit does not change a kernel)."""
     import re
     h = hashlib.sha256()
-    for name in ("ccl.cu", "ccl_kernels.cuh"):
-        with open(os.path.join(ROOT, "connected_component_labelling_gb300", "csrc", name)) as f:
+    csrc = os.path.join(ROOT, "connected_component_labelling_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if not name.endswith((".cu", ".cuh")):
+            continue
+        with open(os.path.join(csrc, name)) as f:
             text = f.read()
         text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)   # block comments
         text = re.sub(r"//[^\n]*", " ", text)                 # line comments

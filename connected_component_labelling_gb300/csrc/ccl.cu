@@ -1,6 +1,7 @@
 // ccl.cu -- host side of the GB300 connected-component labelling library:
 // argument checks, workspace layout, launches and the C ABI of include/ccl.h.
-// The kernels and their design notes are in ccl_kernels.cuh.
+// The kernels and their design notes are in ccl_label_kernels.cuh and
+// ccl_stats_kernels.cuh.
 
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -11,7 +12,8 @@
 #include <vector>
 
 #include "ccl.h"
-#include "ccl_kernels.cuh"
+#include "ccl_label_kernels.cuh"
+#include "ccl_stats_kernels.cuh"
 
 namespace {
 
@@ -68,7 +70,8 @@ struct Layout {
   long long nTiles;
   long long nChunks;     // batch * H * CPR
   int nScanBlocks;
-  size_t offL16, offBm, offCnt, offBsum, offRec, offList, offBcnt, total;
+  size_t offSm, offFm, offCnt, offBsum, offHdr, offEnt, offLr, offBsl, offBls, offBcnt, offSj, offP, offRL,
+      total;
 };
 
 // exact division by d (1 <= d < 2^31) for dividends below 2^31 (Granlund and
@@ -82,6 +85,10 @@ void magic_divisor(long long d, unsigned long long* magic, int* shift) {
   *magic = ((1ull << (32 + l)) + (unsigned long long)d - 1ull) / (unsigned long long)d;
 }
 
+// Largest image the labelling accepts: keys (raster indices inside an image)
+// are 32-bit, so H*W < 2^32.
+constexpr long long MAX_IMAGE_PIXELS = (1ll << 32) - 1;
+
 int make_layout(int batch, int H, int W, Layout* L) {
   Geom& g = L->g;
   g.H = H;
@@ -90,34 +97,52 @@ int make_layout(int batch, int H, int W, Layout* L) {
   g.tilesX = (int)(((long long)W + TW - 1) / TW);
   g.tilesY = (int)(((long long)H + TH - 1) / TH);
   g.WPR = (int)(((long long)W + 31) / 32);
-  g.CPR = (int)(((long long)W + CHUNK - 1) / CHUNK);
+  g.CPR = g.tilesX;
   g.HW = (long long)H * W;
   g.tilesPerImage = (long long)g.tilesX * g.tilesY;
   L->nTiles = g.tilesPerImage * batch;
   L->nChunks = (long long)batch * H * g.CPR;
+  // per-tile records, sized by the full tile of this image shape
+  const int twf = W < TW ? W : TW, thf = H < TH ? H : TH;
+  const int tw8 = (twf + 7) / 8 * 8;
+  g.ENT = twf * thf;
+  g.LRT = (g.ENT + 31) / 32;
+  g.SL = twf * thf - (twf > 2 ? twf - 2 : 0) * (thf > 2 ? thf - 2 : 0);   // border pixels
+  g.BOFF = thf > 1 ? tw8 : 0;            // a one-row tile's last row is its first
+  g.LOFF = g.BOFF + tw8;
+  g.ROFF = g.LOFF + thf;
+  g.BSLW = (g.ROFF + thf + 7) / 8 * 8;   // 16-byte rows
+  const long long spi = g.tilesPerImage * g.SL;
   const long long nsb = (L->nChunks + SCAN_BLOCK - 1) / SCAN_BLOCK;
-  if (nsb > (1ll << 30) || L->nTiles > (1ll << 31) - 1) return CCL_ERR_TOO_LARGE;
+  // tile indices below 2^31; slot ids inside an image below 2^32
+  if (nsb > (1ll << 30) || L->nTiles > (1ll << 31) - 1 || spi >= (1ll << 32)) return CCL_ERR_TOO_LARGE;
+  g.slotsPerImage = (unsigned)spi;
   L->nScanBlocks = (int)nsb;
   magic_divisor(W, &g.wmagic, &g.wshift);
   magic_divisor(g.tilesPerImage, &g.tmagic, &g.tshift);
   magic_divisor(g.tilesX, &g.xmagic, &g.xshift);
   g.vec_img = 0;
   g.vec_out = 0;
+  g.bgval = 0u;
+  const size_t rows = (size_t)batch * H, nt = (size_t)L->nTiles;
   size_t o = 0;
-  L->offL16 = o;
-  o = align_up(o + (size_t)batch * H * W * sizeof(uint16_t), 256);
-  L->offBm = o;
-  o = align_up(o + (size_t)batch * H * g.WPR * sizeof(uint32_t), 256);
-  L->offCnt = o;
-  o = align_up(o + (size_t)(L->nChunks + 1) * sizeof(uint32_t), 256);
-  L->offBsum = o;
-  o = align_up(o + (size_t)(L->nScanBlocks + 1) * sizeof(uint32_t), 256);
-  L->offRec = o;
-  o = align_up(o + (size_t)L->nTiles * 4 * TH * sizeof(uint32_t), 256);
-  L->offList = o;
-  o = align_up(o + (size_t)L->nTiles * BLCAP * sizeof(uint16_t), 256);
-  L->offBcnt = o;
-  o = align_up(o + (size_t)L->nTiles * sizeof(uint32_t), 256);
+  auto take = [&](size_t* off, size_t bytes) {
+    *off = o;
+    o = align_up(o + bytes, 256);
+  };
+  take(&L->offSm, rows * g.WPR * sizeof(uint32_t));
+  take(&L->offFm, rows * g.WPR * sizeof(uint32_t));
+  take(&L->offCnt, (size_t)(L->nChunks + 1) * sizeof(uint32_t));
+  take(&L->offBsum, (size_t)(L->nScanBlocks + 1) * sizeof(uint32_t));
+  take(&L->offHdr, nt * TH * sizeof(uint16_t));
+  take(&L->offEnt, nt * g.ENT * sizeof(uint16_t));
+  take(&L->offLr, nt * g.LRT * sizeof(uint32_t));
+  take(&L->offBsl, nt * g.BSLW * sizeof(uint16_t));
+  take(&L->offBls, nt * g.SL * sizeof(uint16_t));
+  take(&L->offBcnt, nt * sizeof(uint32_t));
+  take(&L->offSj, nt * SJW * sizeof(uint32_t));
+  take(&L->offP, nt * g.SL * sizeof(unsigned long long));
+  take(&L->offRL, nt * g.SL * sizeof(int32_t));
   L->total = o;
   return CCL_OK;
 }
@@ -129,7 +154,7 @@ int validate(const void* img, int batch, int H, int W, int pb, int conn, int mod
   if (pb < 1 || pb > 4) return CCL_ERR_INVALID_ARG;
   if (conn != 4 && conn != 8) return CCL_ERR_INVALID_ARG;
   if (mode != CCL_MODE_ALL && mode != CCL_MODE_BINARY) return CCL_ERR_INVALID_ARG;
-  if ((long long)H * W >= (1ll << 31)) return CCL_ERR_TOO_LARGE;
+  if ((long long)H * W > MAX_IMAGE_PIXELS) return CCL_ERR_TOO_LARGE;
   if (n_out && ((uintptr_t)n_out & 3)) return CCL_ERR_INVALID_ARG;
   if (batch == 0 || H == 0 || W == 0) {
     *empty = true;
@@ -142,6 +167,10 @@ int validate(const void* img, int batch, int H, int W, int pb, int conn, int mod
   const uintptr_t ia = (uintptr_t)img, ib = ia + n * (uintptr_t)pb;
   const uintptr_t la = (uintptr_t)labels, lb = la + n * 4;
   if (ia < lb && la < ib) return CCL_ERR_INVALID_ARG;   // overlapping buffers
+  if (n_out) {   // the counts are written before the labels: they may share no byte
+    const uintptr_t na = (uintptr_t)n_out, nb = na + (uintptr_t)batch * 4;
+    if (na < lb && la < nb) return CCL_ERR_INVALID_ARG;
+  }
   return CCL_OK;
 }
 
@@ -205,7 +234,7 @@ int device_pool(cudaMemPool_t* out) {
 }
 
 // Kernel templates are instantiated for every pixel width (1, 2, 3, 4 bytes),
-// connectivity (4, 8) and mode (all, binary).
+// connectivity (4, 8) and mode (all, ignoring one value).
 #define CCL_DISPATCH(KERNEL, GRID, BLOCK, ...)                                                        \
   do {                                                                                   \
     const unsigned grid_ = (unsigned)(GRID);                                             \
@@ -234,19 +263,6 @@ int device_pool(cudaMemPool_t* out) {
     }                                                                                    \
   } while (0)
 
-void k_tile_local_dispatch(int pb, int conn, int mode, const void* img, uint16_t* L16, int32_t* P,
-                           uint32_t* bm, uint32_t* cnt, const Border& bd, long long tile0,
-                           long long ntiles, const Geom& g, int cap, int* status, cudaStream_t st) {
-  CCL_DISPATCH(k_tile_local, ntiles, NT, L16, P, bm, cnt, bd, g, cap, status, tile0);
-}
-
-void k_seams_dispatch(int pb, int conn, int mode, const void* img, const uint16_t* L16, int32_t* P,
-                      uint32_t* bm, uint32_t* cnt, const Border& bd, const Layout& L,
-                      const Geom& g, int cap, int* status, cudaStream_t st) {
-  CCL_DISPATCH(k_seams, (L.nTiles + SEAM_WARPS - 1) / SEAM_WARPS, 32 * SEAM_WARPS, L16, P, bm, cnt, bd, g,
-               L.nTiles, cap, status);
-}
-
 // The pipeline's pieces on `st`: `ws` is the workspace (layout L), `status`
 // the device word the kernels flag limits in.
 struct Pipe {
@@ -255,9 +271,8 @@ struct Pipe {
   int32_t* labels;
   int32_t* n_out;
   const Layout* L;
-  uint16_t* L16;
-  uint32_t *bm, *cnt, *bsum;
-  Border bd;
+  Work wk;
+  uint32_t* bsum;
   Geom g;
   int capTile, capImg;
   int* status;
@@ -279,14 +294,21 @@ Pipe make_pipe(const void* img, int batch, int H, int W, int pb, int conn, int m
   q.n_out = n_out;
   q.L = &L;
   char* base = (char*)ws;
-  q.L16 = (uint16_t*)(base + L.offL16);
-  q.bm = (uint32_t*)(base + L.offBm);
-  q.cnt = (uint32_t*)(base + L.offCnt);
+  q.wk.sm = (uint32_t*)(base + L.offSm);
+  q.wk.fm = (uint32_t*)(base + L.offFm);
+  q.wk.cnt = (uint32_t*)(base + L.offCnt);
+  q.wk.hdr = (uint16_t*)(base + L.offHdr);
+  q.wk.ent = (uint16_t*)(base + L.offEnt);
+  q.wk.lr = (uint32_t*)(base + L.offLr);
+  q.wk.bsl = (uint16_t*)(base + L.offBsl);
+  q.wk.bls = (uint16_t*)(base + L.offBls);
+  q.wk.bcnt = (uint32_t*)(base + L.offBcnt);
+  q.wk.sj = (uint32_t*)(base + L.offSj);
+  q.wk.P = (unsigned long long*)(base + L.offP);
+  q.wk.RL = (int32_t*)(base + L.offRL);
   q.bsum = (uint32_t*)(base + L.offBsum);
-  q.bd.rec = (uint32_t*)(base + L.offRec);
-  q.bd.list = (uint16_t*)(base + L.offList);
-  q.bd.cnt = (uint32_t*)(base + L.offBcnt);
-  long long capT = TILE + 1, capI = L.g.HW + 1;
+  // walk caps: the nodes a walk can visit (runs of a tile; slots of the call)
+  long long capT = TILE + 1, capI = (long long)L.g.slotsPerImage + 1;
   const long long user = g_walk_cap;
   if (user > 0) {
     capT = capT < user ? capT : user;
@@ -310,30 +332,38 @@ Pipe make_pipe(const void* img, int batch, int H, int W, int pb, int conn, int m
 
 // Start + Connect + Collapse for tiles [tile0, tile0 + ntiles)
 void launch_tile_local(const Pipe& q, long long tile0, long long ntiles) {
-  k_tile_local_dispatch(q.pb, q.conn, q.mode, q.img, q.L16, q.labels, q.bm, q.cnt, q.bd, tile0, ntiles,
-                        q.g, q.capTile, q.status, q.st);
+  const int pb = q.pb, conn = q.conn, mode = q.mode;
+  const void* img = q.img;
+  cudaStream_t st = q.st;
+  CCL_DISPATCH(k_tile_local, ntiles, NT, q.wk, q.g, q.capTile, q.status, tile0);
 }
 void launch_seams(const Pipe& q) {
-  k_seams_dispatch(q.pb, q.conn, q.mode, q.img, q.L16, q.labels, q.bm, q.cnt, q.bd, *q.L, q.g, q.capImg,
-                   q.status, q.st);
+  const unsigned grid = (unsigned)((q.L->nTiles + SEAM_WARPS - 1) / SEAM_WARPS);
+  if (q.conn == 8)
+    k_seams<8><<<grid, 32 * SEAM_WARPS, 0, q.st>>>(q.wk, q.g, q.L->nTiles, q.capImg, q.status);
+  else
+    k_seams<4><<<grid, 32 * SEAM_WARPS, 0, q.st>>>(q.wk, q.g, q.L->nTiles, q.capImg, q.status);
 }
 void launch_scan(const Pipe& q) {
   const Layout& L = *q.L;
-  k_scan_reduce<<<L.nScanBlocks, NT, 0, q.st>>>(q.cnt, L.nChunks, q.bsum);
+  k_scan_reduce<<<L.nScanBlocks, NT, 0, q.st>>>(q.wk.cnt, L.nChunks, q.bsum);
   k_scan_top<<<1, NT, 0, q.st>>>(q.bsum, L.nScanBlocks);
-  k_scan_down<<<L.nScanBlocks, NT, 0, q.st>>>(q.cnt, L.nChunks, q.bsum);
+  k_scan_down<<<L.nScanBlocks, NT, 0, q.st>>>(q.wk.cnt, L.nChunks, q.bsum);
   if (q.n_out)
-    k_region_counts<<<(q.batch + 255) / 256, 256, 0, q.st>>>(q.cnt, (long long)q.H * L.g.CPR, q.batch,
-                                                             q.n_out);
+    k_region_counts<<<(q.batch + 255) / 256, 256, 0, q.st>>>(q.wk.cnt, (long long)q.H * L.g.CPR, q.batch,
+                                                             q.n_out, q.status);
 }
 void launch_resolve(const Pipe& q) {
   const Layout& L = *q.L;
   k_resolve<<<(unsigned)((L.nTiles + RESOLVE_WARPS - 1) / RESOLVE_WARPS), 32 * RESOLVE_WARPS, 0, q.st>>>(
-      q.bd, L.nTiles, q.labels, q.bm, q.cnt, q.g, q.capImg, q.status);
+      q.wk, q.g, L.nTiles, q.capImg, q.status);
 }
 // Number for tiles [tile0, tile0 + ntiles)
 void launch_number(const Pipe& q, long long tile0, long long ntiles) {
-  k_number<<<(unsigned)ntiles, NT, 0, q.st>>>(q.L16, q.labels, q.bm, q.cnt, q.bd, q.g, q.status, tile0);
+  if (q.mode == CCL_MODE_BINARY)
+    k_number<true><<<(unsigned)ntiles, NT, 0, q.st>>>(q.wk, q.labels, q.g, q.status, tile0);
+  else
+    k_number<false><<<(unsigned)ntiles, NT, 0, q.st>>>(q.wk, q.labels, q.g, q.status, tile0);
 }
 
 // The whole labelling pipeline on `st`; `events` whether the optional
@@ -459,6 +489,15 @@ int run(const void* img, int batch, int H, int W, int pb, int conn, int mode, in
   return run_pipeline(img, batch, H, W, pb, conn, mode, 0u, labels, n_out, L, ws, status, true, st);
 }
 
+// the ccl_status a device status word stands for
+int status_of_flags(int h) {
+  if (h & (FLAG_WALK_CAP | FLAG_INTERNAL)) return CCL_ERR_DEVICE_LIMIT;
+  if (h & FLAG_LABEL_RANGE) return CCL_ERR_TOO_LARGE;
+  if (h & FLAG_STATS_CAP) return CCL_ERR_NO_MEMORY;
+  if (h & FLAG_BAD_LABEL) return CCL_ERR_INVALID_ARG;
+  return CCL_OK;
+}
+
 int empty_call(int batch, int32_t* n_out, cudaStream_t st) {
   if (n_out && batch > 0)
     if (cudaMemsetAsync(n_out, 0, (size_t)batch * sizeof(int32_t), st) != cudaSuccess)
@@ -532,7 +571,7 @@ size_t ccl_workspace_bytes(int batch, int H, int W, int pixel_bytes, int connect
   if (pixel_bytes < 1 || pixel_bytes > 4) return 0;
   if (connectivity != 4 && connectivity != 8) return 0;
   if (mode != CCL_MODE_ALL && mode != CCL_MODE_BINARY) return 0;
-  if ((long long)H * W >= (1ll << 31)) return 0;
+  if ((long long)H * W > MAX_IMAGE_PIXELS) return 0;
   Layout L;
   if (make_layout(batch, H, W, &L) != CCL_OK) return 0;
   return L.total;
@@ -646,8 +685,9 @@ int ccl_label_host(const void* img_host, int batch, int H, int W, int pixel_byte
   const size_t imgBytes = align_up(npx * pixel_bytes, 256);
   const size_t labBytes = align_up(npx * 4, 256);
   const size_t nBytes = align_up((size_t)batch * 4, 256);
+  constexpr size_t statusBytes = 256;
   char* buf = nullptr;
-  if (cudaMallocFromPoolAsync((void**)&buf, imgBytes + labBytes + nBytes + L.total, pool, st) !=
+  if (cudaMallocFromPoolAsync((void**)&buf, imgBytes + labBytes + nBytes + statusBytes + L.total, pool, st) !=
       cudaSuccess) {
     cudaGetLastError();
     return CCL_ERR_NO_MEMORY;
@@ -655,17 +695,25 @@ int ccl_label_host(const void* img_host, int batch, int H, int W, int pixel_byte
   void* dImg = buf;
   int32_t* dLab = (int32_t*)(buf + imgBytes);
   int32_t* dN = (int32_t*)(buf + imgBytes + labBytes);
-  void* ws = buf + imgBytes + labBytes + nBytes;
-  int* status = nullptr;
+  // this call's own status word: limits tripped by calls on other streams
+  // stay in the device's sticky word for ccl_last_status
+  int* status = (int*)(buf + imgBytes + labBytes + nBytes);
+  void* ws = buf + imgBytes + labBytes + nBytes + statusBytes;
   cudaStream_t cs = nullptr;
-  rc = device_status_ptr(&status);
+  rc = cudaMemsetAsync(status, 0, sizeof(int), st) == cudaSuccess ? CCL_OK : CCL_ERR_CUDA;
   if (rc == CCL_OK) rc = device_copy_stream(&cs);
   if (rc == CCL_OK)
     rc = run_host_banded(img_host, batch, H, W, pixel_bytes, connectivity, mode, labels_host,
                          n_regions_host, dImg, dLab, dN, L, ws, status, st, cs);
+  int h = 0;
+  if (rc == CCL_OK && cudaMemcpyAsync(&h, status, sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    rc = CCL_ERR_CUDA;
   cudaFreeAsync(buf, st);
-  const int sync = ccl_last_status(stream);
-  return rc != CCL_OK ? rc : sync;
+  if (cudaStreamSynchronize(st) != cudaSuccess) {
+    cudaGetLastError();
+    return CCL_ERR_CUDA;
+  }
+  return rc != CCL_OK ? rc : status_of_flags(h);
 }
 
 int ccl_last_status(ccl_stream_t stream) {
@@ -680,10 +728,7 @@ int ccl_last_status(ccl_stream_t stream) {
   int h = 0;
   if (cudaMemcpy(&h, status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return CCL_ERR_CUDA;
   if (h != 0 && cudaMemset(status, 0, sizeof(int)) != cudaSuccess) return CCL_ERR_CUDA;
-  if (h & (FLAG_WALK_CAP | FLAG_INTERNAL)) return CCL_ERR_DEVICE_LIMIT;
-  if (h & FLAG_STATS_CAP) return CCL_ERR_NO_MEMORY;
-  if (h & FLAG_BAD_LABEL) return CCL_ERR_INVALID_ARG;
-  return CCL_OK;
+  return status_of_flags(h);
 }
 
 int ccl_debug_counters(unsigned long long* out, int n, int reset) {
