@@ -32,6 +32,7 @@ constexpr unsigned FULL = 0xffffffffu;
 static_assert(PX == 8, "a lane owns 8 pixels");
 static_assert(RPW == 2, "a warp owns two consecutive tile rows");
 static_assert(TILE <= 4096, "run ids and their rows share 16 bits");
+static_assert(NT == TW, "a thread per tile column in the border records");
 
 constexpr int FLAG_WALK_CAP = 1;    // a union-find walk or retry loop hit its cap
 constexpr int FLAG_INTERNAL = 2;    // an invariant of the pipeline failed

@@ -182,7 +182,8 @@ __global__ void __launch_bounds__(NT, 8) k_tile_local(const T* __restrict__ img,
   __shared__ int spre[TH][WPT];                          // starts before word m of row r
   __shared__ int rcnt[TH];
   __shared__ int rbS[TH + 1];                            // runs before row r
-  __shared__ uint32_t lrs[LRW], bmark[LRW];              // leaders; leaders of border regions
+  __shared__ uint32_t lrs[LRW], bmark[LRW], bcol[LRW];   // leaders; leaders of border regions;
+                                                         // runs on the first or last column
   __shared__ int nb;
 
   const long long tile = tile0 + blockIdx.x;   // launches may cover a band of tiles
@@ -194,7 +195,10 @@ __global__ void __launch_bounds__(NT, 8) k_tile_local(const T* __restrict__ img,
   // every run is its own set; nothing marked yet; rows below the tile empty
   for (int i = threadIdx.x; i < TILE / 4; i += NT)
     reinterpret_cast<int4*>(par)[i] = make_int4(4 * i, 4 * i + 1, 4 * i + 2, 4 * i + 3);
-  if (threadIdx.x < LRW) bmark[threadIdx.x] = 0u;
+  if (threadIdx.x < LRW) {
+    bmark[threadIdx.x] = 0u;
+    bcol[threadIdx.x] = 0u;
+  }
   if (threadIdx.x == 0) nb = 0;
   if (threadIdx.x < TH * WPT) {
     const int r = threadIdx.x / WPT, m = threadIdx.x % WPT;
@@ -363,6 +367,22 @@ __global__ void __launch_bounds__(NT, 8) k_tile_local(const T* __restrict__ img,
   const int rbx = rinc - rc;   // rb[lane] for lane < TH
   const int total = __shfl_sync(FULL, rinc, TH - 1);
   if (warp == 0 && lane <= TH) rbS[lane] = lane < TH ? rbx : total;
+  // the runs of the inner rows that touch the first or the last column (all
+  // runs of the first and the last row touch the border)
+  if (warp == NWARPS - 1) {
+    const int r = lane & (TH - 1);
+    const int rb0 = __shfl_sync(FULL, rbx, r);
+    const int rbs = __shfl_sync(FULL, rbx, (r + 1) & (TH - 1));   // every lane takes part
+    const int rbn = r + 1 < TH ? rbs : total;
+    if (r > 0 && r < t.th - 1) {
+      if (lane < TH) {
+        if (sw[r][0] & 1u) atomicOr(&bcol[rb0 >> 5], 1u << (rb0 & 31));
+      } else {
+        const bool f = !BIN || ((fw[BIN ? r : 0][(t.tw - 1) >> 5] >> ((t.tw - 1) & 31)) & 1u);
+        if (f) atomicOr(&bcol[(rbn - 1) >> 5], 1u << ((rbn - 1) & 31));
+      }
+    }
+  }
 #pragma unroll
   for (int k = 0; k < RPW; ++k) {
     const int r = warp * RPW + k;
@@ -401,7 +421,9 @@ __global__ void __launch_bounds__(NT, 8) k_tile_local(const T* __restrict__ img,
   __syncthreads();
 
   // ---- Collapse: every run points straight at its tile-local leader; the
-  // leaders are the runs that are their own leader
+  // leaders are the runs that are their own leader.  The leaders of regions
+  // that touch the tile border are marked.
+  const int rbFirst = rbS[1], rbLast = rbS[t.th - 1];   // runs of the first row: [0, rbFirst)
   for (int base = warp * 32; base < total; base += NT) {   // warp-uniform bounds
     const int q = base + lane;
     const bool v = q < total;
@@ -410,6 +432,8 @@ __global__ void __launch_bounds__(NT, 8) k_tile_local(const T* __restrict__ img,
       root = find_s(par, q, cap, status);
       st_relaxed_cta(par + q, root);
       wk.ent[tile * g.ENT + q] = (uint16_t)root;
+      if (q < rbFirst || q >= rbLast || ((bcol[q >> 5] >> (q & 31)) & 1u))
+        atomicOr(&bmark[root >> 5], 1u << (root & 31));
     }
     const unsigned bal = __ballot_sync(FULL, v && root == q);
     if (lane == 0) {
@@ -417,97 +441,48 @@ __global__ void __launch_bounds__(NT, 8) k_tile_local(const T* __restrict__ img,
       wk.lr[tile * g.LRT + (base >> 5)] = bal;
     }
   }
-  // ---- and the leaders of the regions that touch the tile border, marked
-  auto mark = [&](int q) {
-    const int root = find_s(par, q, cap, status);
-    atomicOr(&bmark[root >> 5], 1u << (root & 31));
-  };
-#pragma unroll
-  for (int k = 0; k < RPW; ++k) {
-    const int r = warp * RPW + k;
-    if (r >= t.th || (r != 0 && r != t.th - 1)) continue;   // warp-uniform
-    const int m = lane >> 2, sh = 8 * (lane & 3);
-    const int base = rbS[r] + spre[r][m] + __popc(sw[r][m] & ((1u << sh) - 1u));
-    const unsigned st = stm[k], fg = fgm[k];
-    // the runs with pixels in this lane: the one going on from the left, if
-    // any, and one per start
-    const int hi = base + __popc(st);
-    for (int q = base - (((fg & 1u) && !(st & 1u)) ? 1 : 0); q < hi; ++q) mark(q);
-  }
-  if (warp == NWARPS - 1) {   // first column (lanes 0..15), last column (16..31)
-    const int r = lane & (TH - 1);
-    if (r < t.th) {
-      if (lane < TH) {
-        if (sw[r][0] & 1u) mark(rbS[r]);
-      } else {
-        const bool f = !BIN || ((fw[BIN ? r : 0][(t.tw - 1) >> 5] >> ((t.tw - 1) & 31)) & 1u);
-        if (f) mark(rbS[r + 1] - 1);
+  __syncthreads();
+
+  // ---- a slot for every marked leader: its parent entry names itself, with
+  // its key, the raster position of its first pixel (its run's rank in the
+  // row stands for the column: ranks keep the order, and x0 + rank < x0 +
+  // width, the next tile's first column), and its run and row
+  uint16_t* slotOf = &jl[0][0];   // TILE entries
+  for (int base = warp * 32; base < total; base += NT) {   // warp-uniform bounds
+    const int q = base + lane;
+    const bool mk = q < total && ((bmark[q >> 5] >> (q & 31)) & 1u);
+    const unsigned bal = __ballot_sync(FULL, mk);
+    if (bal) {   // warp-uniform
+      int k0 = 0;
+      if (lane == 0) k0 = atomicAdd(&nb, __popc(bal));
+      k0 = __shfl_sync(FULL, k0, 0);
+      if (mk) {
+        const int k = k0 + __popc(bal & ((1u << lane) - 1u));
+        const int r = row_of_run(rbS, q);
+        const long long gi = tile * g.SL + k;   // entry index; the slot's id in its image:
+        const uint32_t sid = (uint32_t)(gi - (long long)t.b * g.slotsPerImage);
+        const uint32_t key = (uint32_t)((long long)(t.y0 + r) * g.W + t.x0 + (q - rbS[r]));
+        wk.P[gi] = ((unsigned long long)key << 32) | sid;
+        wk.bls[gi] = (uint16_t)(q | (r << 12));
+        slotOf[q] = (uint16_t)k;
       }
     }
   }
   __syncthreads();
 
-  // ---- slots for the marked leaders: parent entry (key = image raster index
-  // of the leader's first pixel), leader run and row
-  uint16_t* slotOf = &jl[0][0];   // TILE entries
-  const int nw = (total + 31) >> 5;
-  if (threadIdx.x < LRW) {   // warps 0..3, a word each
-    const int i = threadIdx.x;
-    unsigned m = i < nw ? bmark[i] : 0u;
-    const int n = __popc(m);
-    int inc = n;
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-      const int v = __shfl_up_sync(FULL, inc, d);
-      if (lane >= d) inc += v;
-    }
-    int wbase = 0;
-    if (lane == 31) wbase = atomicAdd(&nb, inc);
-    int k = __shfl_sync(FULL, wbase, 31) + inc - n;
-    while (m) {
-      const int bb = __ffs(m) - 1;
-      m &= m - 1;
-      const int q = i * 32 + bb;
-      const int r = row_of_run(rbS, q);
-      const int kr = q - rbS[r];   // rank of the run in its row
-      int wd = 0;
-#pragma unroll
-      for (int s = WPT / 2; s > 0; s >>= 1)
-        if (spre[r][wd + s] <= kr) wd += s;
-      const int x = wd * 32 + select_bit(sw[r][wd], kr - spre[r][wd]);
-      const long long gi = tile * g.SL + k;   // entry index; the slot's id in its image:
-      const uint32_t sid = (uint32_t)(gi - (long long)t.b * g.slotsPerImage);
-      const uint32_t key = (uint32_t)((long long)(t.y0 + r) * g.W + t.x0 + x);
-      wk.P[gi] = ((unsigned long long)key << 32) | sid;
-      wk.bls[gi] = (uint16_t)(q | (r << 12));
-      slotOf[q] = (uint16_t)k;
-      ++k;
-    }
-  }
-  __syncthreads();
-
-  // ---- the tile's records: border pixels' slots, run bases, slot count,
-  // leaders per chunk of a row
+  // ---- the tile's records: border pixels' slots (a thread per column for
+  // the first and last rows), run bases, slot count, leaders per chunk
   uint16_t* bs = wk.bsl + tile * g.BSLW;
+  {
+    const int x = threadIdx.x;   // NT == TW
+    if (x < t.tw) {
 #pragma unroll
-  for (int k = 0; k < RPW; ++k) {
-    const int r = warp * RPW + k;
-    if (r >= t.th || (r != 0 && r != t.th - 1)) continue;   // warp-uniform
-    const int m = lane >> 2, sh = 8 * (lane & 3);
-    int id = rbS[r] + spre[r][m] + __popc(sw[r][m] & ((1u << sh) - 1u)) - 1;
-    const unsigned st = stm[k], fg = fgm[k];
-    uint32_t o[PX / 2];
-#pragma unroll
-    for (int j = 0; j < PX; ++j) {
-      if ((st >> j) & 1u) ++id;
-      const uint32_t s = ((fg >> j) & 1u) ? (uint32_t)slotOf[par[id]] : (uint32_t)NOSLOT;
-      if (j & 1) o[j >> 1] |= s << 16;
-      else o[j >> 1] = s;
-    }
-    if (xl < t.tw) {
-      const uint4 v = make_uint4(o[0], o[1], o[2], o[3]);
-      if (r == 0) *reinterpret_cast<uint4*>(bs + xl) = v;
-      if (r == t.th - 1) *reinterpret_cast<uint4*>(bs + g.BOFF + xl) = v;
+      for (int e = 0; e < 2; ++e) {
+        const int r = e == 0 ? 0 : t.th - 1;
+        const bool f = !BIN || ((fw[BIN ? r : 0][x >> 5] >> (x & 31)) & 1u);
+        const int id = rbS[r] + spre[r][x >> 5] + __popc(sw[r][x >> 5] & upto(x & 31)) - 1;
+        bs[(e == 0 ? 0 : g.BOFF) + x] = f ? slotOf[par[id]] : NOSLOT;
+      }
     }
   }
   if (warp == NWARPS - 1) {
@@ -770,8 +745,8 @@ __global__ void __launch_bounds__(32 * RESOLVE_WARPS) k_resolve(Work wk, Geom g,
 
 // Number: the tile's leaders take 1 + the leaders before them in raster
 // order (chunk offset + rank among the chunk's leaders), leaders linked
-// across a seam the label k_resolve found, every other run its leader's
-// label, every pixel its run's.
+// across a seam the label k_resolve found; every run takes its leader's
+// label and every pixel its run's.
 template <bool BIN>
 __global__ void __launch_bounds__(NT, 8) k_number(Work wk, int32_t* labels, Geom g, int* status,
                                                long long tile0) {
@@ -782,12 +757,17 @@ __global__ void __launch_bounds__(NT, 8) k_number(Work wk, int32_t* labels, Geom
   __shared__ uint32_t lrS[LRW];
   __shared__ int rbS[TH + 1];
   __shared__ uint32_t offS[TH];
+  constexpr int PRE = 4;   // runs a thread prefetches the leader of
   const long long tile = tile0 + blockIdx.x;   // launches may cover a band of tiles
   const TileCoord t = tile_coord_of(g, tile);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, xl = lane * PX;
   const long long rowoff0 = (long long)t.b * g.H;
-  const int total = wk.hdr[tile * TH + TH - 1];
-  const int nw = (total + 31) >> 5;
+  const uint16_t* ent = wk.ent + tile * g.ENT;
+  // every load of the tile's records is issued before the first barrier
+  // (entries past the tile's runs are read but never used)
+  int pe[PRE];
+#pragma unroll
+  for (int i = 0; i < PRE; ++i) pe[i] = tid + i * NT < g.ENT ? __ldg(ent + tid + i * NT) : 0;
   if (tid < TH * WPT) {   // the rows' start (and foreground) bits, prefix counts per word
     const int r = tid / WPT, m = tid % WPT;
     uint32_t w = 0u, f = 0u;
@@ -808,7 +788,7 @@ __global__ void __launch_bounds__(NT, 8) k_number(Work wk, int32_t* labels, Geom
     if (BIN) fwS[r][m] = f;
   } else {
     const int i = tid - TH * WPT;
-    if (i < nw) lrS[i] = __ldg(wk.lr + tile * g.LRT + i);
+    if (i < g.LRT) lrS[i] = __ldg(wk.lr + tile * g.LRT + i);
     if (i < TH) rbS[i + 1] = __ldg(wk.hdr + tile * TH + i);
     if (i == TH) rbS[0] = 0;
     if (i >= 32 && i < 32 + TH) {
@@ -825,21 +805,37 @@ __global__ void __launch_bounds__(NT, 8) k_number(Work wk, int32_t* labels, Geom
     }
   }
   __syncthreads();
-  if (tid < nw) {   // the leaders' labels
-    unsigned m = lrS[tid];
-    while (m) {
-      const int b = __ffs(m) - 1;
-      m &= m - 1;
-      const int q = tid * 32 + b;
-      const int r = row_of_run(rbS, q);
-      const uint32_t lab = offS[r] + (uint32_t)range_popc(lrS, rbS[r], q) + 1u;
-      if (lab > (uint32_t)INT_MAX) raise_flag(status, FLAG_LABEL_RANGE);
-      runLab[q] = (int)lab;
+  // the leaders still in the leader bits, row by row (a warp per row of its
+  // own): 1 + the chunk's offset + the leaders before them in the row
+#pragma unroll
+  for (int k = 0; k < RPW; ++k) {
+    const int r = warp * RPW + k;
+    if (r >= t.th) continue;   // warp-uniform
+    const int re = rbS[r + 1];
+    uint32_t lab = offS[r] + 1u;
+    for (int q0 = rbS[r]; q0 < re; q0 += 32) {   // warp-uniform bounds
+      const int q = q0 + lane;
+      const bool lead = q < re && ((lrS[q >> 5] >> (q & 31)) & 1u);
+      const unsigned bal = __ballot_sync(FULL, lead);
+      if (lead) {
+        const uint32_t v = lab + (uint32_t)__popc(bal & ((1u << lane) - 1u));
+        if (v > (uint32_t)INT_MAX) raise_flag(status, FLAG_LABEL_RANGE);
+        runLab[q] = (int)v;
+      }
+      lab += (uint32_t)__popc(bal);
     }
   }
   __syncthreads();
-  for (int q = tid; q < total; q += NT) {   // every other run: its leader's
-    const int e = __ldg(wk.ent + tile * g.ENT + q);
+  // every other run: its leader's label (a leader linked across a seam holds
+  // the label written with the tile's records above)
+  const int total = rbS[TH];
+#pragma unroll
+  for (int i = 0; i < PRE; ++i) {
+    const int q = tid + i * NT;
+    if (q < total && pe[i] != q) runLab[q] = runLab[pe[i]];
+  }
+  for (int q = tid + PRE * NT; q < total; q += NT) {
+    const int e = __ldg(ent + q);
     if (e != q) runLab[q] = runLab[e];
   }
   __syncthreads();
