@@ -13,9 +13,11 @@ Prints ONE JSON line (rank 0).  Device time: CUDA events on the launching
 stream around exactly K steps, inputs resident in HBM.  Per-stage times come
 from CUDA events the library records on the same stream (option
 CCL_OPT_STAGE_EVENTS).  e2e: the same metric through ccl_label_host with
-page-locked host buffers, host<->device copies inside the timed region.
-cpu_baseline / --impl reference: the oracle (single-threaded BFS) on a band of
-the same sheet, on this machine's host cores.
+page-locked host buffers, host<->device copies inside the timed region, with
+the same copies timed alone beside it (the link's floor).  cpu_baseline: the
+oracle (single-threaded BFS) over the whole workload on this machine's host
+cores; its labels and counts are compared with the device run's, every pixel
+("parity").  --impl reference: the oracle on a band of the sheet.
 """
 from __future__ import annotations
 
@@ -39,7 +41,6 @@ FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 8000.0          # the GB300's nominal HBM3e bandwidth, for the second fraction
 L2_BYTES = 129 * 1024 * 1024
 REF_ROWS = 1200           # rows of the sheet one reference step labels
-CPU_BASELINE_ROWS = 9600  # rows of the sheet the cpu_baseline leg labels
 
 
 # ------------------------------------------------------------------ workloads
@@ -334,7 +335,8 @@ def main():
     px = B * H * W
     labels = torch.empty(px, dtype=torch.int32, device=dev)
     nreg = torch.empty(B, dtype=torch.int32, device=dev)
-    wsb = ccl.ccl_workspace_bytes(B, H, W, pb, conn, max(mode, 0))
+    # (ignoring one value is the binary mode's pipeline: its workspace size)
+    wsb = ccl.ccl_workspace_bytes(B, H, W, pb, conn, 1 if mode != 0 else 0)
     ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     sp = stream.cuda_stream
@@ -416,8 +418,8 @@ def main():
     # bytes per pixel charged to the stages that stream whole images:
     # tile_local carries the method's figure (image read once + int32 labels
     # written), the per-unit figure of the roofline when it dominates; number
-    # its own least traffic (leader map read, 2 B, + labels written, 4 B)
-    alg = {"tile_local": pb + 4, "number": 2 + 4}
+    # its own least traffic (labels written, 4 B)
+    alg = {"tile_local": pb + 4, "number": 4}
     dom = max(range(len(per_call)), key=lambda k: per_call[k]) if per_call else 0
     dom_name = names[dom] if names else "tile_local"
     dom_alg = alg.get(dom_name)
@@ -509,7 +511,8 @@ def main():
         counters["tile_links_per_px"] = c["tile_links"] / px
         counters["build"] = "libccl_counters.so (-DCCL_COUNTERS), one call, not timed"
 
-    # ---- e2e through the host entry point
+    # ---- e2e through the host entry point, and the copies alone (the link's
+    # floor for the same bytes: the image up, the labels down)
     e2e = None
     if not args.no_e2e and mode >= 0:
         himg = img.cpu().contiguous().pin_memory()
@@ -520,6 +523,20 @@ def main():
         if rc != ccl.CCL_OK:
             raise ccl.CCLError(rc, "ccl_label_host")
         torch.cuda.synchronize(dev)
+        dimg = torch.empty_like(img)
+        up_ms, down_ms = [], []
+        for _ in range(args.e2e_steps):
+            a, b, c = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+            a.record(stream)
+            dimg.copy_(himg.view(dimg.shape), non_blocking=True)
+            b.record(stream)
+            hlab.copy_(labels, non_blocking=True)
+            c.record(stream)
+            torch.cuda.synchronize(dev)
+            up_ms.append(a.elapsed_time(b))
+            down_ms.append(b.elapsed_time(c))
+        del dimg
+        floor_ms = statistics.median(up_ms) + statistics.median(down_ms)
         barrier(world)
         t0 = time.perf_counter()
         for _ in range(args.e2e_steps):
@@ -533,28 +550,42 @@ def main():
         e2e = {"value": world * px / dt / 1e9, "unit": UNIT, "ms_per_step": dt * 1e3,
                "h2d_bytes_per_step": px * pb, "d2h_bytes_per_step": px * 4 + B * 4,
                "steps": args.e2e_steps, "api": "ccl_label_host (pinned host buffers)",
-               "labels_match_device_run": same}
+               "labels_match_device_run": same,
+               "copy_floor_ms": floor_ms, "h2d_ms": statistics.median(up_ms),
+               "d2h_ms": statistics.median(down_ms), "frac_of_floor": floor_ms / (dt * 1e3),
+               "floor_note": "the same pinned buffers copied alone in this process (image up, "
+                             "then labels down, median of the e2e steps); frac_of_floor = "
+                             "copy_floor_ms / ms_per_step"}
         del himg, hlab
 
-    # ---- cpu baseline: the oracle on a band of the sheet, this host, 1 thread
+    # ---- cpu baseline and parity: the oracle over the whole workload on this
+    # host (1 thread), its labels and counts compared with the device run's
     cpu_baseline = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline and args.workload.startswith("c4"):
+    parity = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
         import oracle
         oracle.build()
-        if pb == 3:   # [1, H, W, 3] bytes
-            band = img[:, :CPU_BASELINE_ROWS].cpu().numpy()
+        if pb == 3:   # [B, H, W, 3] bytes
+            himg_np = img.cpu().numpy().reshape(B, H, W, 3)
         else:
-            band = img[:CPU_BASELINE_ROWS].cpu().numpy().view(np.uint32)
+            himg_np = img.cpu().numpy().view({1: np.uint8, 2: np.uint16, 4: np.uint32}[pb])
+            himg_np = himg_np.reshape(B, H, W)
+        t0 = time.perf_counter()
         if mode < 0:
-            t0 = time.perf_counter()
-            oracle.label_ignore(band, int(cfg["ignore_value"], 16), 8)
-            dt = time.perf_counter() - t0
+            olab, on = oracle.label_ignore(himg_np, int(cfg["ignore_value"], 16), conn)
         else:
-            dt = time_oracle(band, 8, oracle.MODE_ALL)
-        band_px = band.size // 3 if pb == 3 else band.size
-        cpu_baseline = {"value": band_px / dt / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
-                        "sample": "rows 0-%d of the sheet (%d px), one single-threaded BFS pass, "
-                                  "%.1f s" % (CPU_BASELINE_ROWS, band_px, dt),
+            olab, on = oracle.label(himg_np, conn, oracle.MODE_BINARY if mode == 1 else oracle.MODE_ALL)
+        dt = time.perf_counter() - t0
+        del himg_np
+        dlab = labels.cpu().numpy()
+        labels_equal = bool(np.array_equal(olab.reshape(-1), dlab))
+        counts_equal = bool(np.array_equal(np.asarray(on).reshape(-1), np.asarray(n_regions)))
+        parity = {"labels_equal": labels_equal, "counts_equal": counts_equal, "pixels": px,
+                  "against": "oracle (plain BFS, CPU), every pixel of the last timed call's labels"}
+        del olab, dlab
+        cpu_baseline = {"value": px / dt / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
+                        "sample": "the whole workload (%d px), one single-threaded BFS pass, %.1f s"
+                                  % (px, dt),
                         "host": host_info()}
 
     if rank == 0:
@@ -568,7 +599,8 @@ def main():
                                         % (px * (pb + 4) / 1e9)),
                                parallelism="replicas" if world > 1 else "single"),
                 "roofline": roofline, "roofline_path": roofline_path, "stages": stages,
-                "cpu_baseline": cpu_baseline, "e2e": e2e, "gpu_launches": launches,
+                "parity": (parity["labels_equal"] and parity["counts_equal"]) if parity else None,
+                "parity_detail": parity, "cpu_baseline": cpu_baseline, "e2e": e2e, "gpu_launches": launches,
                 "region_stats": region_stats, "counters": counters,
                 "clocks": clocks, "n_regions": n_regions[:8],
                 "kernel_source_sha": source_sha()}

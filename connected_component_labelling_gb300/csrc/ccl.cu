@@ -70,8 +70,7 @@ struct Layout {
   long long nTiles;
   long long nChunks;     // batch * H * CPR
   int nScanBlocks;
-  size_t offSm, offFm, offCnt, offBsum, offHdr, offEnt, offLr, offBsl, offBls, offBcnt, offSj, offP, offRL,
-      total;
+  size_t offSm, offFm, offCnt, offBsum, offHdr, offEnt, offLr, offBsl, offBls, offBcnt, offSj, offP, total;
 };
 
 // exact division by d (1 <= d < 2^31) for dividends below 2^31 (Granlund and
@@ -89,7 +88,8 @@ void magic_divisor(long long d, unsigned long long* magic, int* shift) {
 // are 32-bit, so H*W < 2^32.
 constexpr long long MAX_IMAGE_PIXELS = (1ll << 32) - 1;
 
-int make_layout(int batch, int H, int W, Layout* L) {
+// `fg`: the ignoring modes, which keep foreground bits too
+int make_layout(int batch, int H, int W, bool fg, Layout* L) {
   Geom& g = L->g;
   g.H = H;
   g.W = W;
@@ -112,6 +112,8 @@ int make_layout(int batch, int H, int W, Layout* L) {
   g.LOFF = g.BOFF + tw8;
   g.ROFF = g.LOFF + thf;
   g.BSLW = (g.ROFF + thf + 7) / 8 * 8;   // 16-byte rows
+  g.SJL = (twf + PX - 1) / PX;           // a word per lane with pixels, then the first column's 3
+  g.SJW = g.SJL + 3;
   const long long spi = g.tilesPerImage * g.SL;
   const long long nsb = (L->nChunks + SCAN_BLOCK - 1) / SCAN_BLOCK;
   // tile indices below 2^31; slot ids inside an image below 2^32
@@ -131,7 +133,7 @@ int make_layout(int batch, int H, int W, Layout* L) {
     o = align_up(o + bytes, 256);
   };
   take(&L->offSm, rows * g.WPR * sizeof(uint32_t));
-  take(&L->offFm, rows * g.WPR * sizeof(uint32_t));
+  take(&L->offFm, fg ? rows * g.WPR * sizeof(uint32_t) : 0);
   take(&L->offCnt, (size_t)(L->nChunks + 1) * sizeof(uint32_t));
   take(&L->offBsum, (size_t)(L->nScanBlocks + 1) * sizeof(uint32_t));
   take(&L->offHdr, nt * TH * sizeof(uint16_t));
@@ -140,9 +142,8 @@ int make_layout(int batch, int H, int W, Layout* L) {
   take(&L->offBsl, nt * g.BSLW * sizeof(uint16_t));
   take(&L->offBls, nt * g.SL * sizeof(uint16_t));
   take(&L->offBcnt, nt * sizeof(uint32_t));
-  take(&L->offSj, nt * SJW * sizeof(uint32_t));
+  take(&L->offSj, nt * g.SJW * sizeof(uint32_t));
   take(&L->offP, nt * g.SL * sizeof(unsigned long long));
-  take(&L->offRL, nt * g.SL * sizeof(int32_t));
   L->total = o;
   return CCL_OK;
 }
@@ -305,7 +306,6 @@ Pipe make_pipe(const void* img, int batch, int H, int W, int pb, int conn, int m
   q.wk.bcnt = (uint32_t*)(base + L.offBcnt);
   q.wk.sj = (uint32_t*)(base + L.offSj);
   q.wk.P = (unsigned long long*)(base + L.offP);
-  q.wk.RL = (int32_t*)(base + L.offRL);
   q.bsum = (uint32_t*)(base + L.offBsum);
   // walk caps: the nodes a walk can visit (runs of a tile; slots of the call)
   long long capT = TILE + 1, capI = (long long)L.g.slotsPerImage + 1;
@@ -356,7 +356,7 @@ void launch_scan(const Pipe& q) {
 void launch_resolve(const Pipe& q) {
   const Layout& L = *q.L;
   k_resolve<<<(unsigned)((L.nTiles + RESOLVE_WARPS - 1) / RESOLVE_WARPS), 32 * RESOLVE_WARPS, 0, q.st>>>(
-      q.wk, q.g, L.nTiles, q.capImg, q.status);
+      q.wk, q.labels, q.g, L.nTiles, q.capImg, q.status);
 }
 // Number for tiles [tile0, tile0 + ntiles)
 void launch_number(const Pipe& q, long long tile0, long long ntiles) {
@@ -573,7 +573,7 @@ size_t ccl_workspace_bytes(int batch, int H, int W, int pixel_bytes, int connect
   if (mode != CCL_MODE_ALL && mode != CCL_MODE_BINARY) return 0;
   if ((long long)H * W > MAX_IMAGE_PIXELS) return 0;
   Layout L;
-  if (make_layout(batch, H, W, &L) != CCL_OK) return 0;
+  if (make_layout(batch, H, W, mode == CCL_MODE_BINARY, &L) != CCL_OK) return 0;
   return L.total;
 }
 
@@ -587,7 +587,7 @@ int ccl_label_ws(const void* img, int batch, int H, int W, int pixel_bytes, int 
   cudaStream_t st = (cudaStream_t)stream;
   if (empty) return empty_call(batch, n_regions_out, st);
   Layout L;
-  rc = make_layout(batch, H, W, &L);
+  rc = make_layout(batch, H, W, mode == CCL_MODE_BINARY, &L);
   if (rc != CCL_OK) return rc;
   if (!workspace || ((uintptr_t)workspace & 255)) return CCL_ERR_INVALID_ARG;
   if (workspace_bytes < L.total) return CCL_ERR_NO_MEMORY;
@@ -606,7 +606,7 @@ int ccl_label(const void* img, int batch, int H, int W, int pixel_bytes, int con
   cudaStream_t st = (cudaStream_t)stream;
   if (empty) return empty_call(batch, n_regions_out, st);
   Layout L;
-  rc = make_layout(batch, H, W, &L);
+  rc = make_layout(batch, H, W, mode == CCL_MODE_BINARY, &L);
   if (rc != CCL_OK) return rc;
   cudaMemPool_t pool;
   rc = device_pool(&pool);
@@ -632,7 +632,7 @@ int ccl_label_ignore(const void* img, int batch, int H, int W, int pixel_bytes, 
   cudaStream_t st = (cudaStream_t)stream;
   if (empty) return empty_call(batch, n_regions_out, st);
   Layout L;
-  rc = make_layout(batch, H, W, &L);
+  rc = make_layout(batch, H, W, true, &L);
   if (rc != CCL_OK) return rc;
   if (workspace) {
     if ((uintptr_t)workspace & 255) return CCL_ERR_INVALID_ARG;
@@ -676,7 +676,7 @@ int ccl_label_host(const void* img_host, int batch, int H, int W, int pixel_byte
   }
   cudaStream_t st = (cudaStream_t)stream;
   Layout L;
-  rc = make_layout(batch, H, W, &L);
+  rc = make_layout(batch, H, W, mode == CCL_MODE_BINARY, &L);
   if (rc != CCL_OK) return rc;
   cudaMemPool_t pool;
   rc = device_pool(&pool);
@@ -771,7 +771,7 @@ int ccl_region_stats(const int32_t* labels_i32, int batch, int H, int W, const i
     if (workspace_bytes < need) return CCL_ERR_NO_MEMORY;
   }
   Layout L;
-  int rc = make_layout(batch, H, W, &L);
+  int rc = make_layout(batch, H, W, false, &L);
   if (rc != CCL_OK) return rc;
   Geom g = L.g;
   g.vec_out = (W % 8 == 0) && ((uintptr_t)labels_i32 % 16 == 0);
@@ -865,7 +865,7 @@ extern "C" int ccl_label_noalloc(const void* img, int batch, int H, int W, int p
   cudaStream_t st = (cudaStream_t)stream;
   if (empty) return empty_call(batch, n_regions_out, st);
   Layout L;
-  rc = make_layout(batch, H, W, &L);
+  rc = make_layout(batch, H, W, mode == CCL_MODE_BINARY, &L);
   if (rc != CCL_OK) return rc;
   if (L.total > (size_t)CCL_NOALLOC_SCRATCH_BYTES - NOALLOC_STATUS_BYTES) return CCL_ERR_TOO_LARGE;
   char* scratch = nullptr;

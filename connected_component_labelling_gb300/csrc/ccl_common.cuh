@@ -23,7 +23,6 @@ constexpr int WPT = TW / 32;        // bit-mask words per tile row
 constexpr int LRW = TILE / 32;      // leader-run words per tile
 constexpr int BLCAP = 2 * TW + 2 * TH;   // border slots per tile (>= border pixels)
 constexpr int NBSL = 2 * TW + 2 * TH;    // border pixels of a tile record
-constexpr int SJW = 40;             // seam join words per tile
 constexpr int JCAP = 2 * TW;        // joins of one row (at most two per pixel)
 constexpr int SCAN_ITEMS = 16;
 constexpr int SCAN_BLOCK = NT * SCAN_ITEMS;
@@ -60,6 +59,7 @@ struct Geom {
   int SL;                       // slots per tile: border pixels of a full tile
   int BSLW;                     // border-record entries per tile
   int BOFF, LOFF, ROFF;         // last row, first column, last column in a record
+  int SJW, SJL;                 // seam-join words per tile; the first column's start at SJL
   unsigned slotsPerImage;       // tilesPerImage * SL (< 2^32)
   int vec_img;                  // image rows allow 8-pixel vector loads
   int vec_out;                  // label rows allow 16-byte vector stores

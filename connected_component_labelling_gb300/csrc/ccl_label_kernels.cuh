@@ -57,9 +57,8 @@ struct Work {
                             //   first row, last row (at BOFF), first column (LOFF), last column (ROFF)
   uint16_t* bls;            // [nTiles][SL] leader run of every slot | its row << 12
   uint32_t* bcnt;           // [nTiles] slots used
-  uint32_t* sj;             // [nTiles][SJW] seam joins: first row (a word per lane), first column
+  uint32_t* sj;             // [nTiles][SJW] seam joins: first row (a word per lane), first column (at SJL)
   unsigned long long* P;    // [nTiles][SL] parent entry of every slot: key << 32 | parent slot
-  int32_t* RL;              // [nTiles][SL] label of a slot linked under another region
 };
 // Slots are numbered inside their image (tile of the image * SL + place in
 // the tile): the entries of image b start at index b * slotsPerImage.
@@ -295,7 +294,7 @@ __global__ void __launch_bounds__(NT, 8) k_tile_local(const T* __restrict__ img,
       }
     }
     if (r == 0) {   // the first row's joins are the top seam's: k_seams makes them
-      if (up) wk.sj[tile * SJW + lane] = todo;
+      if (up && lane < g.SJL) wk.sj[tile * g.SJW + lane] = todo;
       todo = 0u;
     }
     stm[k] = starts;
@@ -348,9 +347,10 @@ __global__ void __launch_bounds__(NT, 8) k_tile_local(const T* __restrict__ img,
     const bool urb = CONN == 8 && v && r >= 1 && fq && q == pu && q != qu;
     const unsigned bl = __ballot_sync(FULL, lb), bul = __ballot_sync(FULL, ulb), bur = __ballot_sync(FULL, urb);
     if (lane == 0) {
-      wk.sj[tile * SJW + 32] = bl;
-      wk.sj[tile * SJW + 33] = bul;
-      wk.sj[tile * SJW + 34] = bur;
+      uint32_t* sj = wk.sj + tile * g.SJW + g.SJL;
+      sj[0] = bl;
+      sj[1] = bul;
+      sj[2] = bur;
     }
   }
   __syncthreads();
@@ -557,7 +557,7 @@ __global__ void __launch_bounds__(32 * SEAM_WARPS) k_seams(Work wk, Geom g, long
 
   // ---- top seam
   if (t.y0 > 0) {
-    const unsigned todo0 = wk.sj[tile * SJW + lane];
+    const unsigned todo0 = lane < g.SJL ? wk.sj[tile * g.SJW + lane] : 0u;
     if (__any_sync(FULL, todo0 != 0u)) {
       const long long ta = tile - g.tilesX;   // the tile above (always full height)
       if (xl < t.tw) {
@@ -583,8 +583,8 @@ __global__ void __launch_bounds__(32 * SEAM_WARPS) k_seams(Work wk, Geom g, long
   }
   // ---- left seam
   if (t.x0 > 0) {
-    const uint32_t* sj = wk.sj + tile * SJW;
-    const uint32_t bl = sj[32], bul = sj[33], bur = sj[34];
+    const uint32_t* sj = wk.sj + tile * g.SJW + g.SJL;
+    const uint32_t bl = sj[0], bul = sj[1], bur = sj[2];
     const int r = lane;
     const bool v = r < t.th;
     const unsigned so = v ? wk.bsl[tile * g.BSLW + g.LOFF + r] : NOSLOT;
@@ -720,17 +720,25 @@ __device__ __forceinline__ int label_of_root(const Work& wk, uint32_t s, int b, 
 
 constexpr int RESOLVE_WARPS = 2;   // tiles (a warp each) per block: small blocks free their slot sooner
 
+// The label found for slot k of a tile waits in the labels buffer, inside
+// that tile (k < the tile's pixels), until k_number reads it back before it
+// writes the tile.
+__device__ __forceinline__ long long parked_label_index(const TileCoord& t, const Geom& g, int k) {
+  const int ry = k / t.tw;
+  return ((long long)t.b * g.H + t.y0 + ry) * g.W + t.x0 + (k - ry * t.tw);
+}
+
 // Collapse + Number for the border leaders linked across seams (a warp per
 // tile, a lane per slot): each walks to its region's root (halving on the
-// way) and stores the root's label for its slot.
-__global__ void __launch_bounds__(32 * RESOLVE_WARPS) k_resolve(Work wk, Geom g, long long nTiles, int cap,
-                                                                int* status) {
+// way) and parks the root's label for its slot.
+__global__ void __launch_bounds__(32 * RESOLVE_WARPS) k_resolve(Work wk, int32_t* labels, Geom g,
+                                                                long long nTiles, int cap, int* status) {
   const long long tile = (long long)blockIdx.x * RESOLVE_WARPS + (threadIdx.x >> 5);
   if (tile >= nTiles) return;
   const int lane = threadIdx.x & 31;
-  const int b = (int)(tile / g.tilesPerImage);
-  unsigned long long* Pi = wk.P + (long long)b * g.slotsPerImage;
-  const uint32_t s0 = (uint32_t)((tile - (long long)b * g.tilesPerImage) * g.SL);
+  const TileCoord t = tile_coord_of(g, tile);
+  unsigned long long* Pi = wk.P + (long long)t.b * g.slotsPerImage;
+  const uint32_t s0 = (uint32_t)((tile - (long long)t.b * g.tilesPerImage) * g.SL);
   const int count = min((int)wk.bcnt[tile], g.SL);
   for (int k = lane; k < count; k += 32) {
     const uint32_t s = s0 + k;
@@ -739,7 +747,7 @@ __global__ void __launch_bounds__(32 * RESOLVE_WARPS) k_resolve(Work wk, Geom g,
     CCL_COUNT(CCL_CNT_RESOLVE_STEPS);
     const unsigned long long rv = find_g(Pi, s, g.slotsPerImage, cap, status);
     if (rv == NOENTRY) continue;
-    wk.RL[tile * g.SL + k] = label_of_root(wk, (uint32_t)rv, b, g, status);
+    labels[parked_label_index(t, g, k)] = label_of_root(wk, (uint32_t)rv, t.b, g, status);
   }
 }
 
@@ -796,12 +804,12 @@ __global__ void __launch_bounds__(NT, 8) k_number(Work wk, int32_t* labels, Geom
       const long long img0 = rowoff0 * g.CPR;
       offS[r] = r < t.th ? __ldg(wk.cnt + (rowoff0 + t.y0 + r) * g.CPR + t.tx) - __ldg(wk.cnt + img0) : 0u;
     }
-    // leaders linked across a seam: the label k_resolve stored for their slot
+    // leaders linked across a seam: the label k_resolve parked for their slot
     const int count = min((int)__ldg(wk.bcnt + tile), g.SL);
     const uint32_t s0 = (uint32_t)((tile - (long long)t.b * g.tilesPerImage) * g.SL);
     for (int k = i; k < count; k += NT - TH * WPT) {
       const long long gi = tile * g.SL + k;
-      if ((uint32_t)__ldg(wk.P + gi) != s0 + k) runLab[__ldg(wk.bls + gi) & 0xFFF] = __ldg(wk.RL + gi);
+      if ((uint32_t)__ldg(wk.P + gi) != s0 + k) runLab[__ldg(wk.bls + gi) & 0xFFF] = labels[parked_label_index(t, g, k)];
     }
   }
   __syncthreads();

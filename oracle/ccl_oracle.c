@@ -30,11 +30,13 @@
  */
 #include <stdint.h>
 #include <stdlib.h>
+#include <limits.h>
 #include <string.h>
 
 /* Return codes mirror the library's status numbers where they overlap. */
 #define ORACLE_OK 0
 #define ORACLE_ERR_INVALID_ARG 1
+#define ORACLE_ERR_TOO_LARGE 2   /* H*W >= 2^32, or more regions than int32 labels hold */
 #define ORACLE_ERR_NO_MEMORY 4
 
 enum { ORACLE_MODE_ALL = 0, ORACLE_MODE_BINARY = 1 };
@@ -52,7 +54,7 @@ static int is_zero(const uint8_t* a, int pb) {
 /*
  * Label one image.  img: H*W pixels of pb bytes, row-major.  labels: H*W
  * int32, written completely.  queue: scratch of H*W int64.  Returns the
- * number of regions.
+ * number of regions, or -1 if they outnumber what int32 labels hold.
  */
 static int64_t label_one(const uint8_t* img, int64_t H, int64_t W, int pb,
                          int conn, int mode, const uint8_t* ign,
@@ -79,6 +81,7 @@ static int64_t label_one(const uint8_t* img, int64_t H, int64_t W, int pb,
   int64_t n = 0;
   for (int64_t seed = 0; seed < N; ++seed) {
     if (labels[seed] != -1) continue;
+    if (n == INT32_MAX) return -1;   /* one more region than int32 labels hold */
     ++n;
     labels[seed] = (int32_t)n;
     int64_t head = 0, tail = 0;
@@ -105,8 +108,10 @@ static int64_t label_one(const uint8_t* img, int64_t H, int64_t W, int pb,
  * oracle_label: label `batch` images of H x W pixels of `pixel_bytes` bytes,
  * stored contiguously; image b starts at byte b*H*W*pixel_bytes and its labels
  * at element b*H*W.  n_out[b] receives the number of regions of image b.
- * Host pointers only.  Returns ORACLE_OK, ORACLE_ERR_INVALID_ARG or
- * ORACLE_ERR_NO_MEMORY.
+ * Host pointers only.  Images of up to 2^32 - 1 pixels (64-bit indices
+ * throughout).  Returns ORACLE_OK, ORACLE_ERR_INVALID_ARG,
+ * ORACLE_ERR_NO_MEMORY, or ORACLE_ERR_TOO_LARGE (H*W >= 2^32, or an image
+ * with more regions than int32 labels hold: its count is -1).
  */
 static int label_all(const void* img, int64_t batch, int64_t H, int64_t W,
                      int pixel_bytes, int connectivity, int mode,
@@ -149,17 +154,20 @@ static int label_all(const void* img, int64_t batch, int64_t H, int64_t W,
     return ORACLE_OK;
   }
   if (!img || !labels || !n_out) return ORACLE_ERR_INVALID_ARG;
-  if (N >= ((int64_t)1 << 31)) return ORACLE_ERR_INVALID_ARG;
+  /* the library's bound: raster indices inside an image fit 32 bits */
+  if (N >= ((int64_t)1 << 32)) return ORACLE_ERR_TOO_LARGE;
   int64_t* queue = (int64_t*)malloc((size_t)N * sizeof(int64_t));
   if (!queue) return ORACLE_ERR_NO_MEMORY;
   const uint8_t* base = (const uint8_t*)img;
+  int rc = ORACLE_OK;
   for (int64_t b = 0; b < batch; ++b) {
-    n_out[b] = (int32_t)label_one(base + b * N * pixel_bytes, H, W,
-                                  pixel_bytes, connectivity, mode, ign,
-                                  labels + b * N, queue);
+    const int64_t n = label_one(base + b * N * pixel_bytes, H, W, pixel_bytes,
+                                connectivity, mode, ign, labels + b * N, queue);
+    if (n < 0) rc = ORACLE_ERR_TOO_LARGE;
+    n_out[b] = n < 0 ? -1 : (int32_t)n;
   }
   free(queue);
-  return ORACLE_OK;
+  return rc;
 }
 
 /*

@@ -55,13 +55,17 @@ def test_workspace_bytes(lib):
     assert ccl.ccl_workspace_bytes(1, 10, 10, 5, 8, 0) == 0       # bad pixel_bytes
     assert ccl.ccl_workspace_bytes(1, 10, 10, 3, 8, 0) > 0        # 24-bit RGB
     assert ccl.ccl_workspace_bytes(1, 10, 10, 1, 6, 0) == 0       # bad connectivity
-    assert ccl.ccl_workspace_bytes(1, 1 << 16, 1 << 15, 1, 8, 0) == 0   # H*W = 2^31
+    assert ccl.ccl_workspace_bytes(1, 1 << 16, 1 << 15, 1, 8, 0) > 0    # H*W = 2^31 is accepted
+    assert ccl.ccl_workspace_bytes(1, 1 << 16, 1 << 16, 1, 8, 0) == 0   # H*W = 2^32 is not
     a = ccl.ccl_workspace_bytes(1, 1024, 1024, 4, 8, 0)
     b = ccl.ccl_workspace_bytes(2, 1024, 1024, 4, 8, 0)
     assert 0 < a < b
-    # 2-byte leader map + bitmap (1 bit/px) + chunk counts + border records and lists
+    # run start bits (1 bit/px) + per 256 x 16 tile: run bases, a leader per run
+    # (4096 x 2 B), leader bits, border records, slot parents (540 x 8 B) ...
     px = 1024 * 1024
-    assert 2 * px + px // 8 <= a < 3 * px
+    assert 3.5 * px <= a < 4.5 * px
+    # the ignoring modes add foreground bits (1 bit/px)
+    assert ccl.ccl_workspace_bytes(1, 1024, 1024, 4, 8, 1) == a + px // 8
     assert a % 256 == 0
 
 
@@ -77,7 +81,7 @@ FAKE = 1 << 20   # a host address never dereferenced: validation fails first
     ((FAKE, 1, -8, 8, 1, 8, 0), ccl.CCL_ERR_INVALID_ARG),    # H
     ((None, 1, 8, 8, 1, 8, 0), ccl.CCL_ERR_INVALID_ARG),     # null image
     ((FAKE + 1, 1, 8, 8, 4, 8, 0), ccl.CCL_ERR_INVALID_ARG), # misaligned RGBA
-    ((FAKE, 1, 1 << 16, 1 << 15, 1, 8, 0), ccl.CCL_ERR_TOO_LARGE),
+    ((FAKE, 1, 1 << 16, 1 << 16, 1, 8, 0), ccl.CCL_ERR_TOO_LARGE),   # H*W = 2^32
 ])
 def test_invalid_arguments_rejected_on_host(lib, args, expect):
     img, B, H, W, pb, conn, mode = args
@@ -109,6 +113,7 @@ def test_null_labels_and_overlap_rejected(lib):
 
 def test_workspace_checks_on_host(lib):
     need = ccl.ccl_workspace_bytes(1, 64, 64, 1, 8, 0)
+    need_ign = ccl.ccl_workspace_bytes(1, 64, 64, 1, 8, 1)   # ignoring: the binary mode's size
     args = (FAKE, 1, 64, 64, 1, 8, 0, FAKE * 64, None)
     assert ccl.ccl_label_ws(*args, FAKE * 128, need - 1, None) == ccl.CCL_ERR_NO_MEMORY
     assert ccl.ccl_label_ws(*args, FAKE * 128 + 16, need, None) == ccl.CCL_ERR_INVALID_ARG
@@ -121,7 +126,7 @@ def test_workspace_checks_on_host(lib):
                labels + 4096 * 4 - 256):            # from the labels' last bytes on
         ws -= ws % 256
         assert ccl.ccl_label_ws(*base, None, ws, need, None) == ccl.CCL_ERR_INVALID_ARG, hex(ws)
-        assert ccl.ccl_label_ignore(*base[:6], 5, labels, None, ws, need, None) == \
+        assert ccl.ccl_label_ignore(*base[:6], 5, labels, None, ws, need_ign, None) == \
             ccl.CCL_ERR_INVALID_ARG, hex(ws)
     assert need % 256 == 0
     ws = counts + 256 - need                        # its last 256 bytes hold the counts
@@ -199,15 +204,20 @@ def test_plain_c_consumer_links_and_runs(lib, tmp_path):
 
 
 def test_workspace_bytes_of_the_largest_shapes(lib):
-    """Geometry near 2^31 is computed in 64 bits: the one-row image of
-    2^31 - 1 pixels needs about 7.4 B/px (the per-tile border lists of its
-    8.4 M one-row tiles), the square just below 2^31 pixels about 2.5 B/px,
-    and 2^31 pixels are refused."""
+    """Geometry is computed in 64 bits and every per-tile record is sized by
+    the image's full tile: images of up to 2^32 - 1 pixels are accepted.  A
+    square of many whole tiles needs about 3.9 B/px; the one-row image of
+    2^31 - 1 pixels about 15 B/px (every pixel of its one-row tiles is a
+    border pixel with a possible slot); 2^32 pixels are refused, and so is an
+    image whose tiles' slots would outnumber 32-bit ids (2 rows of 2^31 - 1)."""
     w1 = (1 << 31) - 1
     row = ccl.ccl_workspace_bytes(1, 1, w1, 1, 8, 0)
-    assert 0 < row < 8 * w1
+    assert 0 < row < 16 * w1
     sq = ccl.ccl_workspace_bytes(1, 46340, 46340, 1, 8, 0)
-    assert 2 * 46340 ** 2 < sq < 3 * 46340 ** 2
+    assert 3.5 * 46340 ** 2 < sq < 4.5 * 46340 ** 2
+    big = ccl.ccl_workspace_bytes(1, 65535, 65535, 1, 8, 0)   # 2^32 - 2^17 + 1 pixels
+    assert 3.5 * 65535 ** 2 < big < 4.5 * 65535 ** 2
     col = ccl.ccl_workspace_bytes(1, w1, 1, 1, 8, 0)
     assert col > 0
-    assert ccl.ccl_workspace_bytes(1, 1 << 16, 1 << 15, 1, 8, 0) == 0
+    assert ccl.ccl_workspace_bytes(1, 1 << 16, 1 << 16, 1, 8, 0) == 0
+    assert ccl.ccl_workspace_bytes(1, 2, w1, 1, 8, 0) == 0

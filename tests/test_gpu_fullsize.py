@@ -84,7 +84,8 @@ def test_c4_sheet_paper_ignored():
     # "every-colour", ch. 08 switch 4: the sheet with its white paper ignored
     img = workloads.c4_sheet(device=DEV)
     white = 0xFFFFFFFF
-    need = ccl.ccl_workspace_bytes(1, 24000, 33600, 4, 8, 0)
+    # (ignoring a value runs the binary mode's pipeline: its workspace size)
+    need = ccl.ccl_workspace_bytes(1, 24000, 33600, 4, 8, ccl.CCL_MODE_BINARY)
     ws = torch.empty(need, dtype=torch.uint8, device=DEV)
     lab, n = ccl.label_ignore(img, white, connectivity=8, workspace=ws)
     ccl.check_status()

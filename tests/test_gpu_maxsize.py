@@ -1,9 +1,11 @@
-"""GPU labelling at the largest images the library accepts (H·W just below
-2^31): every raster index, parent slot, leader count and label then sits near
-the top of the int32 range.  The images have closed-form labels, checked
-chunk by chunk on the device (an oracle pass at this size would take minutes,
-and the closed forms are pinned against the oracle at small sizes in
-tests/test_oracle_pins.py)."""
+"""GPU labelling at the largest images: just below 2^31 pixels (labels near
+the top of the int32 range), past 2^31 ("every-colour" ch. 11: images of
+more than 2^31 pixels are the case it never ran) and just below 2^32, the
+largest the library accepts (raster keys inside an image are 32-bit).  The
+images have closed-form labels, checked chunk by chunk on the device (an
+oracle pass at this size would take minutes; the closed forms are pinned
+against the oracle at small sizes in tests/test_oracle_pins.py, and the
+oracle itself past 2^31 there too)."""
 import pytest
 import torch
 
@@ -13,6 +15,8 @@ pytestmark = pytest.mark.gpu
 
 DEV = torch.device("cuda:0")
 N = 46340                      # N * N = 2,147,395,600 < 2^31 - 1
+N2 = 46341                     # N2 * N2 = 2,147,488,281 > 2^31
+N3 = 65535                     # N3 * N3 = 4,294,836,225 < 2^32
 W1 = (1 << 31) - 1             # the widest one-row image
 CHUNK = 2048                   # rows compared at a time
 
@@ -38,9 +42,8 @@ def label_ws(img, conn, mode):
     return lab, n
 
 
-def checkerboard():
-    assert N * N < (1 << 31)
-    r = torch.arange(N, device=DEV, dtype=torch.int32)
+def checkerboard(n=N):
+    r = torch.arange(n, device=DEV, dtype=torch.int32)
     return ((r[:, None] + r[None, :]) & 1).to(torch.uint8)
 
 
@@ -115,3 +118,76 @@ def test_one_row_of_max_width():
     assert int(f["sum_y"].abs().sum()) == 0
     assert torch.equal(f["sum_x"], (x_min + x_max) * area // 2)
     del lab, raw, f
+
+
+def test_checkerboard_8conn_all_beyond_2_31():
+    """Past 2^31 pixels: still the two diagonal families."""
+    img = checkerboard(N2)
+    assert N2 * N2 > (1 << 31)
+    lab, n = label_ws(img, 8, "all")
+    assert int(n) == 2
+    c = torch.arange(N2, device=DEV, dtype=torch.int32)
+    for r0 in range(0, N2, CHUNK):
+        r = torch.arange(r0, min(N2, r0 + CHUNK), device=DEV, dtype=torch.int32)
+        assert torch.equal(lab[r0:r0 + len(r)], 1 + ((r[:, None] + c[None, :]) & 1)), r0
+    del lab, img
+
+
+def test_checkerboard_4conn_binary_beyond_2_31():
+    """Every 1 its own region past 2^31 pixels (N2 odd): rows hold 23170 and
+    23171 ones alternately, so the one at (r, c) is number
+    r*23170 + r//2 + c//2 + 1, the last one (N2*N2 - 1) / 2."""
+    img = checkerboard(N2)
+    lab, n = label_ws(img, 4, "binary")
+    assert int(n) == (N2 * N2 - 1) // 2
+    c = torch.arange(N2, device=DEV, dtype=torch.int64)
+    for r0 in range(0, N2, CHUNK):
+        r = torch.arange(r0, min(N2, r0 + CHUNK), device=DEV, dtype=torch.int64)
+        one = ((r[:, None] + c[None, :]) & 1) == 1
+        exp = torch.where(one, r[:, None] * ((N2 - 1) // 2) + r[:, None] // 2 + c[None, :] // 2 + 1, 0)
+        assert torch.equal(lab[r0:r0 + len(r)], exp.to(torch.int32)), r0
+    del lab, img
+
+
+def test_more_regions_than_int32_labels_reported():
+    """The 4-connected all-pixels checkerboard past 2^31 pixels has N2*N2 >
+    2^31 - 1 regions: more than int32 labels hold.  The call completes and
+    the device status reports CCL_ERR_TOO_LARGE (the counts are clamped)."""
+    img = checkerboard(N2)
+    B, H, W, pb, _ = ccl.image_geometry(img)
+    ws = torch.empty(ccl.ccl_workspace_bytes(B, H, W, pb, 4, 0), dtype=torch.uint8, device=DEV)
+    lab, n = ccl.label(img, 4, "all", workspace=ws)
+    with pytest.raises(ccl.CCLError) as e:
+        ccl.check_status()
+    assert e.value.status == ccl.CCL_ERR_TOO_LARGE
+    assert int(n) == (1 << 31) - 1
+    del lab, ws, img
+
+
+def test_checkerboard_8conn_all_near_2_32():
+    """The largest square accepted, 65535^2 = 2^32 - 2^17 + 1 pixels."""
+    img = checkerboard(N3)
+    lab, n = label_ws(img, 8, "all")
+    assert int(n) == 2
+    c = torch.arange(N3, device=DEV, dtype=torch.int32)
+    for r0 in range(0, N3, CHUNK):
+        r = torch.arange(r0, min(N3, r0 + CHUNK), device=DEV, dtype=torch.int32)
+        assert torch.equal(lab[r0:r0 + len(r)], 1 + ((r[:, None] + c[None, :]) & 1)), r0
+    del lab, img
+
+
+def test_serpentine_binary_near_2_32():
+    """One serpentine of 1s through 65535^2 pixels (even rows all 1, odd rows
+    a single 1 at alternate ends): one region of 2^31 + 2^15 pixels whose
+    joins chain through every tile seam of the image; label 1 on the 1s."""
+    r = torch.arange(N3, device=DEV, dtype=torch.int64)
+    c = torch.arange(N3, device=DEV, dtype=torch.int64)
+    img = torch.zeros((N3, N3), dtype=torch.uint8, device=DEV)
+    img[0::2] = 1
+    img[1::4, N3 - 1] = 1
+    img[3::4, 0] = 1
+    lab, n = label_ws(img, 8, "binary")
+    assert int(n) == 1
+    for r0 in range(0, N3, CHUNK):
+        assert torch.equal(lab[r0:r0 + CHUNK], img[r0:r0 + CHUNK].to(torch.int32)), r0
+    del lab, img, r, c

@@ -359,3 +359,46 @@ def test_ignore_compares_every_byte(tmp_path):
                             ctypes.c_int64(3), 4, 8, ctypes.c_void_p(ign.ctypes.data),
                             ctypes.c_void_p(out.ctypes.data), ctypes.c_void_p(cnt.ctypes.data))
     assert cnt[0] != 1          # the planted mistake is caught
+
+
+def _free_memory_bytes():
+    try:
+        with open("/proc/meminfo") as f:
+            for line in f:
+                if line.startswith("MemAvailable:"):
+                    return int(line.split()[1]) * 1024
+    except OSError:
+        pass
+    return 0
+
+
+def test_image_beyond_2_31_pixels():
+    """"every-colour" ch. 11 names images of more than 2^31 pixels as the case
+    it never ran; the oracle indexes in 64 bits and accepts up to 2^32 - 1
+    pixels.  One row of 2^31 + 3000 pixels in runs of 2^20 of alternating
+    value (4-connectivity): run k is region k + 1, so the last pixels carry
+    a label past 2^11 with raster indices past 2^31.  Needs about 28 GB of
+    host memory (image, labels, the flood fill's queue)."""
+    W = (1 << 31) + 3000
+    if _free_memory_bytes() < 34 * (1 << 30):
+        pytest.skip("needs about 28 GB of free host memory")
+    x = np.arange(W, dtype=np.int64)
+    img = ((x >> 20) & 1).astype(np.uint8).reshape(1, W)
+    del x
+    lab, n = oracle.label(img, 4, oracle.MODE_ALL)
+    del img
+    assert int(n) == (W + (1 << 20) - 1) >> 20
+    step = 1 << 27
+    for x0 in range(0, W, step):
+        xs = np.arange(x0, min(W, x0 + step), dtype=np.int64)
+        np.testing.assert_array_equal(lab[0, x0:x0 + len(xs)], ((xs >> 20) + 1).astype(np.int32))
+
+
+def test_images_of_2_32_pixels_refused():
+    """Images of 2^32 pixels or more are refused (status 2), as by the
+    library; nothing is read (the pointers are never touched)."""
+    import ctypes
+    n = (ctypes.c_int32 * 1)()
+    rc = oracle._load().oracle_label(ctypes.c_void_p(16), 1, 1 << 16, 1 << 16, 1, 4, 0,
+                                     ctypes.c_void_p(16), n)
+    assert rc == 2
