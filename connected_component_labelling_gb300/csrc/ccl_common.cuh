@@ -218,6 +218,7 @@ __device__ __forceinline__ void load8<uint32_t>(const uint32_t* p, bool vec, int
 
 // ------------------------------------------------------------- bit helpers
 
+
 // bits 0..b of a word (b in 0..31)
 __device__ __forceinline__ uint32_t upto(int b) { return (2u << b) - 1u; }
 

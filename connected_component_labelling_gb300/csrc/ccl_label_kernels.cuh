@@ -720,12 +720,12 @@ __device__ __forceinline__ int label_of_root(const Work& wk, uint32_t s, int b, 
 
 constexpr int RESOLVE_WARPS = 2;   // tiles (a warp each) per block: small blocks free their slot sooner
 
-// The label found for slot k of a tile waits in the labels buffer, inside
-// that tile (k < the tile's pixels), until k_number reads it back before it
-// writes the tile.
-__device__ __forceinline__ long long parked_label_index(const TileCoord& t, const Geom& g, int k) {
-  const int ry = k / t.tw;
-  return ((long long)t.b * g.H + t.y0 + ry) * g.W + t.x0 + (k - ry * t.tw);
+// The label found for a leader linked across a seam (run q of its tile)
+// waits in the labels buffer, inside that tile (q < the tile's pixels), until
+// k_number reads it back before it writes the tile.
+__device__ __forceinline__ long long parked_label_index(const TileCoord& t, const Geom& g, int q) {
+  const int ry = q / t.tw;
+  return ((long long)t.b * g.H + t.y0 + ry) * g.W + t.x0 + (q - ry * t.tw);
 }
 
 // Collapse + Number for the border leaders linked across seams (a warp per
@@ -747,7 +747,8 @@ __global__ void __launch_bounds__(32 * RESOLVE_WARPS) k_resolve(Work wk, int32_t
     CCL_COUNT(CCL_CNT_RESOLVE_STEPS);
     const unsigned long long rv = find_g(Pi, s, g.slotsPerImage, cap, status);
     if (rv == NOENTRY) continue;
-    labels[parked_label_index(t, g, k)] = label_of_root(wk, (uint32_t)rv, t.b, g, status);
+    const int q = wk.bls[tile * g.SL + k] & 0xFFF;
+    labels[parked_label_index(t, g, q)] = label_of_root(wk, (uint32_t)rv, t.b, g, status);
   }
 }
 
@@ -772,10 +773,17 @@ __global__ void __launch_bounds__(NT, 8) k_number(Work wk, int32_t* labels, Geom
   const long long rowoff0 = (long long)t.b * g.H;
   const uint16_t* ent = wk.ent + tile * g.ENT;
   // every load of the tile's records is issued before the first barrier
-  // (entries past the tile's runs are read but never used)
+  // (entries past the tile's runs are read but never used): the leaders of
+  // the first PRE * NT runs, and the leader-bit words holding those runs
+  const int total = __ldg(wk.hdr + tile * TH + TH - 1);
   int pe[PRE];
+  uint32_t pl[PRE];
 #pragma unroll
-  for (int i = 0; i < PRE; ++i) pe[i] = tid + i * NT < g.ENT ? __ldg(ent + tid + i * NT) : 0;
+  for (int i = 0; i < PRE; ++i) {
+    const int q = tid + i * NT;
+    pe[i] = q < g.ENT ? __ldg(ent + q) : 0;
+    pl[i] = q < g.ENT ? __ldg(wk.lr + tile * g.LRT + (q >> 5)) : 0u;
+  }
   if (tid < TH * WPT) {   // the rows' start (and foreground) bits, prefix counts per word
     const int r = tid / WPT, m = tid % WPT;
     uint32_t w = 0u, f = 0u;
@@ -804,14 +812,17 @@ __global__ void __launch_bounds__(NT, 8) k_number(Work wk, int32_t* labels, Geom
       const long long img0 = rowoff0 * g.CPR;
       offS[r] = r < t.th ? __ldg(wk.cnt + (rowoff0 + t.y0 + r) * g.CPR + t.tx) - __ldg(wk.cnt + img0) : 0u;
     }
-    // leaders linked across a seam: the label k_resolve parked for their slot
-    const int count = min((int)__ldg(wk.bcnt + tile), g.SL);
-    const uint32_t s0 = (uint32_t)((tile - (long long)t.b * g.tilesPerImage) * g.SL);
-    for (int k = i; k < count; k += NT - TH * WPT) {
-      const long long gi = tile * g.SL + k;
-      if ((uint32_t)__ldg(wk.P + gi) != s0 + k) runLab[__ldg(wk.bls + gi) & 0xFFF] = labels[parked_label_index(t, g, k)];
-    }
   }
+  // leaders linked across a seam (their own leader, out of the leader bits):
+  // the label k_resolve parked in the tile
+#pragma unroll
+  for (int i = 0; i < PRE; ++i) {
+    const int q = tid + i * NT;
+    if (q < total && pe[i] == q && !((pl[i] >> (q & 31)) & 1u)) runLab[q] = labels[parked_label_index(t, g, q)];
+  }
+  for (int q = tid + PRE * NT; q < total; q += NT)
+    if (__ldg(ent + q) == q && !((__ldg(wk.lr + tile * g.LRT + (q >> 5)) >> (q & 31)) & 1u))
+      runLab[q] = labels[parked_label_index(t, g, q)];
   __syncthreads();
   // the leaders still in the leader bits, row by row (a warp per row of its
   // own): 1 + the chunk's offset + the leaders before them in the row
@@ -835,8 +846,7 @@ __global__ void __launch_bounds__(NT, 8) k_number(Work wk, int32_t* labels, Geom
   }
   __syncthreads();
   // every other run: its leader's label (a leader linked across a seam holds
-  // the label written with the tile's records above)
-  const int total = rbS[TH];
+  // the label read back above)
 #pragma unroll
   for (int i = 0; i < PRE; ++i) {
     const int q = tid + i * NT;
