@@ -729,8 +729,13 @@ __device__ __forceinline__ long long parked_label_index(const TileCoord& t, cons
 }
 
 // Collapse + Number for the border leaders linked across seams (a warp per
-// tile, a lane per slot): each walks to its region's root (halving on the
-// way) and parks the root's label for its slot.
+// tile, a lane per slot): each walks to its region's root and parks the
+// root's label for its slot.  After k_seams the entries only change here,
+// and only a root's own: the first walker to reach a root stores the root's
+// label in the entry's upper half (top bit set, in place of the key), so
+// that the other walkers that reach it read the label with the entry.
+constexpr unsigned long long LABELLED = 1ull << 63;
+
 __global__ void __launch_bounds__(32 * RESOLVE_WARPS) k_resolve(Work wk, int32_t* labels, Geom g,
                                                                 long long nTiles, int cap, int* status) {
   const long long tile = (long long)blockIdx.x * RESOLVE_WARPS + (threadIdx.x >> 5);
@@ -738,17 +743,35 @@ __global__ void __launch_bounds__(32 * RESOLVE_WARPS) k_resolve(Work wk, int32_t
   const int lane = threadIdx.x & 31;
   const TileCoord t = tile_coord_of(g, tile);
   unsigned long long* Pi = wk.P + (long long)t.b * g.slotsPerImage;
+  const uint32_t n = g.slotsPerImage;
   const uint32_t s0 = (uint32_t)((tile - (long long)t.b * g.tilesPerImage) * g.SL);
   const int count = min((int)wk.bcnt[tile], g.SL);
   for (int k = lane; k < count; k += 32) {
     const uint32_t s = s0 + k;
-    const unsigned long long v = ld_relaxed_gpu(Pi + s);
+    unsigned long long v = ld_relaxed_gpu(Pi + s);
     if ((uint32_t)v == s) continue;   // still a leader: k_number labels it
     CCL_COUNT(CCL_CNT_RESOLVE_STEPS);
-    const unsigned long long rv = find_g(Pi, s, g.slotsPerImage, cap, status);
-    if (rv == NOENTRY) continue;
     const int q = wk.bls[tile * g.SL + k] & 0xFFF;
-    labels[parked_label_index(t, g, q)] = label_of_root(wk, (uint32_t)rv, t.b, g, status);
+    uint32_t x = (uint32_t)v;
+    int st = 0;
+    for (; st < cap; ++st) {   // to the root (the entries are pointers: no halving here)
+      if (x >= n) break;
+      v = ld_relaxed_gpu(Pi + x);
+      if ((uint32_t)v == x) break;
+      x = (uint32_t)v;
+    }
+    if (st == cap || x >= n) {
+      raise_flag(status, st == cap ? FLAG_WALK_CAP : FLAG_INTERNAL);
+      continue;
+    }
+    int lab;
+    if (v & LABELLED) {
+      lab = (int)((v >> 32) & 0x7FFFFFFFu);
+    } else {
+      lab = label_of_root(wk, x, t.b, g, status);
+      atomicCAS(Pi + x, v, LABELLED | ((unsigned long long)((uint32_t)lab & 0x7FFFFFFFu) << 32) | x);
+    }
+    labels[parked_label_index(t, g, q)] = lab;
   }
 }
 

@@ -109,6 +109,12 @@ def test_null_labels_and_overlap_rejected(lib):
     assert ccl.ccl_label(FAKE, 1, 8, 8, 1, 8, 0, None, None, None) == ccl.CCL_ERR_INVALID_ARG
     # labels overlapping the image
     assert ccl.ccl_label(FAKE, 1, 8, 8, 4, 8, 0, FAKE + 64, None, None) == ccl.CCL_ERR_INVALID_ARG
+    # counts overlapping the labels (the counts are written before the labels)
+    labels = FAKE * 64
+    assert ccl.ccl_label(FAKE, 2, 8, 8, 1, 8, 0, labels, labels + 4 * 127, None) == \
+        ccl.CCL_ERR_INVALID_ARG
+    assert ccl.ccl_label_noalloc(FAKE, 2, 8, 8, 1, 8, 0, labels, labels, None) == \
+        ccl.CCL_ERR_INVALID_ARG
 
 
 def test_workspace_checks_on_host(lib):

@@ -219,6 +219,34 @@ def test_walk_cap_reports_device_limit_without_hanging():
     assert int(n) == 1
 
 
+def test_walk_cap_through_the_host_entry_point():
+    """ccl_label_host returns a limit tripped in its own call directly, and
+    keeps to its own status word: a limit another call tripped stays in the
+    device's sticky word for ccl_last_status, and a clean host call after it
+    still reports CCL_OK."""
+    img = workloads.serpentine(256, 256)
+    himg = img.contiguous().pin_memory()
+    hlab = torch.empty((256, 256), dtype=torch.int32).pin_memory()
+    hn = torch.empty((1,), dtype=torch.int32).pin_memory()
+    st = torch.cuda.current_stream(DEV).cuda_stream
+
+    def host_call():
+        return ccl.ccl_label_host(himg.data_ptr(), 1, 256, 256, 1, 8, ccl.CCL_MODE_BINARY,
+                                  hlab.data_ptr(), hn.data_ptr(), st)
+    try:
+        assert ccl.ccl_set_option(ccl.CCL_OPT_WALK_CAP, 1) == ccl.CCL_OK
+        assert host_call() == ccl.CCL_ERR_DEVICE_LIMIT
+        assert ccl.ccl_last_status(st) == ccl.CCL_OK          # not in the sticky word
+        ccl.label(img.to(DEV), 8, "binary")                   # trips the sticky word
+    finally:
+        ccl.ccl_set_option(ccl.CCL_OPT_WALK_CAP, 0)
+    assert host_call() == ccl.CCL_OK                          # its own word is clean
+    assert int(hn[0]) == 1
+    np.testing.assert_array_equal(hlab.numpy(), img.numpy().astype(np.int32))
+    assert ccl.ccl_last_status(st) == ccl.CCL_ERR_DEVICE_LIMIT   # the other call's finding
+    assert ccl.ccl_last_status(st) == ccl.CCL_OK
+
+
 def test_other_stream_and_batch_offsets():
     imgs = workloads.bernoulli_masks(5, 211, 389, (0.3, 0.5, 0.7), seed=4)
     olab, on = oracle.label(imgs.numpy(), 4, oracle.MODE_BINARY)

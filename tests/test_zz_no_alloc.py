@@ -48,7 +48,7 @@ def test_noalloc_matches_ccl_label_on_consecutive_calls():
 
 
 def test_noalloc_rejects_images_beyond_its_scratch():
-    # 4000 x 4000 needs about 34 MB of scratch, more than the fixed 32 MiB
+    # 4000 x 4000 needs about 64 MB of scratch, more than the fixed 32 MiB
     img = torch.zeros((4000, 4000), dtype=torch.uint8, device=DEV)
     lab = torch.empty((4000, 4000), dtype=torch.int32, device=DEV)
     assert ccl.ccl_workspace_bytes(1, 4000, 4000, 1, 8, 0) > ccl.CCL_NOALLOC_SCRATCH_BYTES - 256
@@ -56,3 +56,23 @@ def test_noalloc_rejects_images_beyond_its_scratch():
         rc = ccl.ccl_label_noalloc(img.data_ptr(), 1, 4000, 4000, 1, 8, 0, lab.data_ptr(), None,
                                    torch.cuda.current_stream(DEV).cuda_stream)
     assert rc == ccl.CCL_ERR_TOO_LARGE
+
+
+def test_noalloc_reports_a_tripped_limit_in_its_counts():
+    """A device limit tripped during a no-alloc call (here a walk cap of one
+    step on a serpentine) comes back as -1 in every count, not through the
+    device's sticky word; the call after it, with the cap restored, starts
+    from a clean status and matches ccl_label again."""
+    ccl.build()
+    img = workloads.serpentine(256, 256).to(DEV)
+    try:
+        assert ccl.ccl_set_option(ccl.CCL_OPT_WALK_CAP, 1) == ccl.CCL_OK
+        _, n = _noalloc(img, 8, ccl.CCL_MODE_BINARY)
+        assert int(n) == -1
+    finally:
+        ccl.ccl_set_option(ccl.CCL_OPT_WALK_CAP, 0)
+    lab, n = _noalloc(img, 8, ccl.CCL_MODE_BINARY)
+    ref_lab, ref_n = ccl.label(img, connectivity=8, mode="binary")
+    ccl.check_status()
+    assert int(n) == int(ref_n) == 1
+    assert torch.equal(lab, ref_lab)
