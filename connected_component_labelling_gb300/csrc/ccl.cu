@@ -796,9 +796,10 @@ int ccl_region_stats(const int32_t* labels_i32, int batch, int H, int W, const i
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     sms = 1;
   k_stats_init<<<(unsigned)(sms * 8), NT, 0, st>>>(stats, (long long)capacity, off, batch, status);
-  const long long areas = (long long)batch * (((long long)H + SR - 1) / SR) * L.g.tilesX;
-  k_region_stats<<<(unsigned)areas, STATS_NT, 0, st>>>(labels_i32, n_regions, off, stats,
-                                                 (long long)capacity, g, status);
+  const int stripsX = (int)(((long long)W + STRIP_W - 1) / STRIP_W);
+  const long long strips = (long long)batch * (((long long)H + SR - 1) / SR) * stripsX;
+  k_region_stats<<<(unsigned)strips, STATS_NT, 0, st>>>(labels_i32, n_regions, off, stats,
+                                                  (long long)capacity, g, stripsX, status);
   g_launches += 3;
   rc = cudaPeekAtLastError() == cudaSuccess ? CCL_OK : CCL_ERR_CUDA;
   if (!workspace && cudaFreeAsync(ws, st) != cudaSuccess && rc == CCL_OK) rc = CCL_ERR_CUDA;

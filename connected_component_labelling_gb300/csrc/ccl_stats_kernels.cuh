@@ -88,201 +88,246 @@ __device__ __forceinline__ void stats_add_global(ccl_region_stat* e, int area, i
   atomicAdd(reinterpret_cast<unsigned long long*>(&e->sum_x), sx);
 }
 
-// A block per 256-column x SR-row area; a warp per row at a time, a lane per
-// 8 consecutive labels (as in k_tile_local).  Each lane splits its labels
-// into runs of equal label; the warp's runs of one label are merged first
-// (lanes grouped by label, their lengths, ends and sums reduced across the
-// group) so that a label updates the area's table once per row.  The table
-// (open addressing on the label) keeps, per label, the area, box, first
-// pixel, coordinate sums and whether any of its pixels lies on an inner edge
-// of the area (a row or column with neighbours outside it).  A label that
-// does not is wholly inside the area -- a region that reaches outside crosses
-// that edge -- so its entry is stored outright; the others are added to the
-// global entry with atomics.  A run whose label finds no free slot goes
-// straight to the global entry.  Every label must be one 4- or 8-connected
-// set, as the labels of this library are.
+// A block per strip of SSEG areas of 256 columns x SR rows, taken one area
+// after another.  A warp takes one row of the area at a time, a lane 8
+// consecutive labels (as in k_tile_local).  The row's runs of equal label
+// (run starts from equal-to-left masks) are listed in shared memory and dealt
+// out to the warp's lanes, a run each, so that busy rows keep every lane
+// working.  Each run updates the area's table (open addressing on the
+// label): pixel count and row and column sums relative to the strip's corner
+// packed in one 64-bit add, smallest and largest column, largest row, first
+// pixel (as row << 11 | column inside the strip), whether any pixel lies on
+// an inner edge of the area and whether on one of the strip (a row or column
+// with neighbours outside it).  A label on no edge of its area is wholly
+// inside it -- a region that reaches outside crosses that edge -- so its
+// entry is stored outright; the others are merged into the strip's table,
+// whose labels on no edge of the strip are stored outright at the end and the
+// rest added to the global entry with atomics: a region crossing many areas
+// (a drawing's paper) then costs one global update per strip, not per area.
+// A run or area entry that finds no free slot goes straight to the global
+// entry.  Every label must be one 4- or 8-connected set, as the labels of
+// this library are.
 #ifndef CCL_STATS_HASH
-#define CCL_STATS_HASH 1024
+#define CCL_STATS_HASH 256
 #define CCL_STATS_ROWS 16
+#define CCL_STATS_SEGS 8
 #define CCL_STATS_NT 256
 #endif
 constexpr int STATS_HASH = CCL_STATS_HASH;
 constexpr int SR = CCL_STATS_ROWS;       // rows of a statistics area
+constexpr int SSEG = CCL_STATS_SEGS;     // areas of a strip
+constexpr int STRIP_W = SSEG * TW;       // columns of a strip
 constexpr int STATS_NT = CCL_STATS_NT;   // threads of a statistics block
 constexpr int STATS_NWARPS = STATS_NT / 32;
-constexpr int STATS_HASH_BITS = STATS_HASH == 4096 ? 12 : STATS_HASH == 2048 ? 11 : STATS_HASH == 1024 ? 10 : 9;
+constexpr int STATS_HASH_BITS = STATS_HASH == 1024 ? 10 : STATS_HASH == 512 ? 9 : 8;
 static_assert((1 << STATS_HASH_BITS) == STATS_HASH, "a power of two");
-constexpr int EDGE_BIT = 1 << 30;   // in a table entry's area word: a pixel on an inner edge
+static_assert(STRIP_W <= 2048 && SR <= 16, "strip columns fit 11 bits, rows 4, in the packed first pixel");
+static_assert(STATS_HASH <= STATS_NT, "a thread per slot when an area's table is emptied");
+// the packed sums of a table slot: column sum (bits 0..25), row sum (26..45),
+// pixel count (46..63), all relative to the strip's corner.  A strip's pixels
+// keep each field below its top: sum of columns <= SR * STRIP_W^2 / 2 < 2^26,
+// of rows <= STRIP_W * SR^2 / 2 < 2^20, count <= SR * STRIP_W < 2^18.
+constexpr int ACC_Y = 26, ACC_N = 46;
+constexpr int FIRST_ROW_SHIFT = 11;
+constexpr uint8_t EDGE_AREA = 1, EDGE_STRIP = 2;
 
-__global__ void __launch_bounds__(STATS_NT) k_region_stats(const int32_t* __restrict__ labels,
+struct StatsTable {
+  int key[STATS_HASH], xmin[STATS_HASH], xmax[STATS_HASH], ymax[STATS_HASH], first[STATS_HASH];
+  unsigned long long acc[STATS_HASH];
+  uint8_t edge[STATS_HASH];
+};
+
+__device__ __forceinline__ void table_clear(StatsTable& t, int i) {
+  t.key[i] = 0;   // labels start at 1
+  t.xmin[i] = INT_MAX;
+  t.xmax[i] = -1;
+  t.ymax[i] = -1;
+  t.first[i] = INT_MAX;
+  t.acc[i] = 0ull;
+  t.edge[i] = 0;
+}
+
+// merge one partial into label l's slot; false when the table is crowded
+__device__ __forceinline__ bool table_add(StatsTable& t, int l, unsigned long long acc, int xmin, int xmax,
+                                          int ymax, int first, uint8_t edge) {
+  unsigned h = ((unsigned)l * 2654435761u) >> (32 - STATS_HASH_BITS);
+  for (int probe = 0; probe < 16; ++probe) {
+    const int prev = atomicCAS(&t.key[h], 0, l);
+    if (prev == 0 || prev == l) {
+      atomicAdd(&t.acc[h], acc);
+      atomicMin(&t.xmin[h], xmin);
+      atomicMax(&t.xmax[h], xmax);
+      atomicMax(&t.ymax[h], ymax);
+      atomicMin(&t.first[h], first);
+      if (edge) atomicOr(reinterpret_cast<unsigned*>(&t.edge[h & ~3u]), (unsigned)edge << (8 * (h & 3u)));
+      return true;
+    }
+    h = (h + 1) & (STATS_HASH - 1);
+  }
+  return false;
+}
+
+// a partial of label l (strip-relative, strip corner (y0, x0)) into its global entry
+__device__ __forceinline__ void partial_to_global(ccl_region_stat* e, unsigned long long acc, int xmin, int xmax,
+                                                  int ymax, int first, int y0, int x0, const Geom& g) {
+  const int area = (int)(acc >> ACC_N);
+  const unsigned long long sy = ((acc >> ACC_Y) & ((1ull << (ACC_N - ACC_Y)) - 1ull)) +
+                                (unsigned long long)y0 * area;
+  const unsigned long long sx = (acc & ((1ull << ACC_Y) - 1ull)) + (unsigned long long)x0 * area;
+  const int ymin = y0 + (first >> FIRST_ROW_SHIFT);
+  stats_add_global(e, area, ymin, x0 + xmin, ymax, x0 + xmax, ymin * g.W + x0 + (first & (STRIP_W - 1)),
+                   sy, sx);
+}
+
+__device__ __forceinline__ void partial_store(ccl_region_stat* e, unsigned long long acc, int xmin, int xmax,
+                                              int ymax, int first, int y0, int x0, const Geom& g) {
+  ccl_region_stat r;
+  r.area = (int)(acc >> ACC_N);
+  r.y_min = y0 + (first >> FIRST_ROW_SHIFT);
+  r.x_min = x0 + xmin;
+  r.y_max = ymax;
+  r.x_max = x0 + xmax;
+  r.first = r.y_min * g.W + x0 + (first & (STRIP_W - 1));
+  r.sum_y = (int64_t)(((acc >> ACC_Y) & ((1ull << (ACC_N - ACC_Y)) - 1ull)) + (unsigned long long)y0 * r.area);
+  r.sum_x = (int64_t)((acc & ((1ull << ACC_Y) - 1ull)) + (unsigned long long)x0 * r.area);
+  *e = r;
+}
+
+__global__ void __launch_bounds__(STATS_NT, 6) k_region_stats(const int32_t* __restrict__ labels,
                                                      const int32_t* __restrict__ n_regions,
                                                      const long long* __restrict__ off,
                                                      ccl_region_stat* stats, long long capacity,
-                                                     Geom g, int* status) {
-  // per slot: label, area (+ EDGE_BIT), smallest / largest column, largest
-  // row, first raster index, and the row and column sums relative to the
-  // area's corner (the smallest row is the first pixel's)
-  __shared__ int hkey[STATS_HASH], harea[STATS_HASH], hxmin[STATS_HASH], hxmax[STATS_HASH];
-  __shared__ int hymax[STATS_HASH], hfirst[STATS_HASH];
-  __shared__ unsigned hsy[STATS_HASH], hsx[STATS_HASH];
-  for (int i = threadIdx.x; i < STATS_HASH; i += STATS_NT) {
-    hkey[i] = 0;   // labels start at 1
-    harea[i] = 0;
-    hxmin[i] = INT_MAX;
-    hxmax[i] = -1;
-    hymax[i] = -1;
-    hfirst[i] = INT_MAX;
-    hsy[i] = 0;
-    hsx[i] = 0;
+                                                     Geom g, int stripsX, int* status) {
+  __shared__ StatsTable ta, ts;                               // the area's and the strip's tables
+  __shared__ __align__(16) int rowS[STATS_NWARPS][TW];        // the warp's row of labels
+  __shared__ uint16_t runS[STATS_NWARPS][TW + 1];             // its runs' first columns
+  // some partial went straight to a global entry (a crowded table): then a
+  // label of the strip's table may have global partials too, so none of that
+  // table's entries is stored outright
+  __shared__ int spilled;
+  if (threadIdx.x < STATS_HASH) {
+    table_clear(ta, threadIdx.x);
+    table_clear(ts, threadIdx.x);
   }
+  if (threadIdx.x == 0) spilled = 0;
   __syncthreads();
-  // block -> image, area row, area column
-  const int areasY = (int)(((long long)g.H + SR - 1) / SR);
-  const long long perImage = (long long)areasY * g.tilesX;
+  // block -> image, strip row, strip column
+  const int stripsY = (int)(((long long)g.H + SR - 1) / SR);
+  const long long perImage = (long long)stripsY * stripsX;
   const int b = (int)(blockIdx.x / perImage);
   const int rest = (int)(blockIdx.x - (long long)b * perImage);
-  const int ay = div_magic(rest, g.xmagic, g.xshift), ax = rest - ay * g.tilesX;
-  const int y0 = ay * SR, y1 = y0 + min(SR, g.H - y0) - 1;   // rows y0..y1
-  const int x0 = ax * TW, x1 = x0 + min(TW, g.W - x0) - 1;   // columns x0..x1
+  const int sy = rest / stripsX, sxi = rest - sy * stripsX;
+  const int y0 = sy * SR, y1 = y0 + min(SR, g.H - y0) - 1;                          // rows y0..y1
+  const int x0 = sxi * STRIP_W, sw = (int)min((long long)STRIP_W, (long long)g.W - x0);   // columns
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, xl = lane * PX;
   const int nb = n_regions[b];
   const long long base = off[b];
   const int32_t* li = labels + (long long)b * g.HW;
-  const int nval = max(0, min(PX, x1 - x0 + 1 - xl));
-  const bool vec = g.vec_out && nval == PX;
-  const unsigned vmask = (1u << nval) - 1u;
-  // inner edges: a pixel there has neighbours outside the area
-  const bool edgeL = x0 > 0, edgeR = x1 < g.W - 1;
-  for (int y = y0 + warp; y <= y1; y += STATS_NWARPS) {
-    const int32_t* row = li + (long long)y * g.W + x0 + xl;
-    int v[PX];
-    if (vec) {
-      const int4 p = __ldg(reinterpret_cast<const int4*>(row));
-      const int4 q = __ldg(reinterpret_cast<const int4*>(row) + 1);
-      v[0] = p.x; v[1] = p.y; v[2] = p.z; v[3] = p.w;
-      v[4] = q.x; v[5] = q.y; v[6] = q.z; v[7] = q.w;
-    } else {
+  const bool topIn = y0 > 0, botIn = y1 < g.H - 1;   // rows with neighbours outside
+  const bool stripL = x0 > 0, stripR = (long long)x0 + sw < g.W;
+  int* rb = rowS[warp];
+  uint16_t* L = runS[warp];
+  const int nseg = (sw + TW - 1) / TW;
+  for (int s = 0; s < nseg; ++s) {
+    const int ax0 = s * TW, aw = min(TW, sw - ax0);   // the area: strip columns ax0 ..
+    const bool areaL = ax0 > 0 || stripL, areaR = ax0 + aw < sw || stripR;
+    const int nval = max(0, min(PX, aw - xl));
+    const bool vec = g.vec_out && nval == PX;
+    const unsigned vmask = (1u << nval) - 1u;
+    for (int y = y0 + warp; y <= y1; y += STATS_NWARPS) {
+      const int32_t* row = li + (long long)y * g.W + x0 + ax0 + xl;
+      int v[PX];
+      if (vec) {
+        const int4 p = __ldg(reinterpret_cast<const int4*>(row));
+        const int4 q = __ldg(reinterpret_cast<const int4*>(row) + 1);
+        v[0] = p.x; v[1] = p.y; v[2] = p.z; v[3] = p.w;
+        v[4] = q.x; v[5] = q.y; v[6] = q.z; v[7] = q.w;
+      } else {
 #pragma unroll
-      for (int j = 0; j < PX; ++j) v[j] = j < nval ? __ldg(row + j) : 0;
-    }
-    const bool edgeRow = (y == y0 && y0 > 0) || (y == y1 && y1 < g.H - 1);
-    // runs of equal label inside the lane
-    unsigned same = 0;   // bit j: v[j] == v[j-1]
-#pragma unroll
-    for (int j = 1; j < PX; ++j) same |= (v[j] == v[j - 1] ? 1u : 0u) << j;
-    const unsigned starts = vmask & ~same;
-    // an end: the next label differs, or the pixel is the lane's last valid one
-    unsigned ends = vmask & (~(same >> 1) | (vmask ^ (vmask >> 1)));
-    // A run that crosses from lane L into lanes L+1.. is counted once, by
-    // lane L: a segmented suffix sum over the lanes gathers the pieces of
-    // the lanes it continues into (each lane's first run, while the lanes
-    // it passes through hold nothing else).
-    const int lastv = nval > 0 ? v[nval - 1] : 0;
-    const int prevLast = __shfl_up_sync(FULL, lastv, 1);
-    const bool contL = lane > 0 && nval > 0 && v[0] == prevLast;   // my first run began to my left
-    const bool single = __popc(ends) == 1;
-    const int e0 = ends ? __ffs(ends) - 1 : 0;                      // end of my first run
-    const bool contNext = __shfl_down_sync(FULL, contL ? 1 : 0, 1) != 0 && lane < 31;
-    // the piece I hand to the lane on my left, and whether the chain goes on past me
-    unsigned pl = contL ? (unsigned)(e0 + 1) : 0u;                   // length
-    unsigned px = contL ? (unsigned)(2 * xl + e0) * (unsigned)(e0 + 1) / 2u : 0u;   // column sum
-    unsigned pm = contL ? (unsigned)(xl + e0) : 0u;                  // last column
-    unsigned pe = (contL && ((xl + e0 == x1 - x0 && edgeR) || edgeRow)) ? 1u : 0u;
-    bool brk = !(single && contNext);
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const unsigned nl = __shfl_down_sync(FULL, pl, o), nx = __shfl_down_sync(FULL, px, o);
-      const unsigned nm = __shfl_down_sync(FULL, pm, o), ne = __shfl_down_sync(FULL, pe, o);
-      const bool nb2 = __shfl_down_sync(FULL, brk ? 1 : 0, o) != 0;
-      if (!brk && lane + o < 32) {
-        pl += nl;
-        px += nx;
-        pm = max(pm, nm);
-        pe |= ne;
-        brk = nb2;
+        for (int j = 0; j < PX; ++j) v[j] = j < nval ? __ldg(row + j) : 0;
       }
-    }
-    // the chain that continues my last run: the sums from lane + 1
-    const unsigned cl = __shfl_down_sync(FULL, pl, 1), cx = __shfl_down_sync(FULL, px, 1);
-    const unsigned cm = __shfl_down_sync(FULL, pm, 1), ce = __shfl_down_sync(FULL, pe, 1);
-    bool firstRun = true;
-    while (ends) {
-      const int e = __ffs(ends) - 1;
-      ends &= ends - 1;
-      const bool isFirst = firstRun;
-      firstRun = false;
-      if (isFirst && contL) continue;   // counted by the lane where the run began
-      const int sj = 31 - __clz(starts & ((2u << e) - 1u));
-      int l = 0;
+      const int vl = __shfl_up_sync(FULL, v[PX - 1], 1);
+      unsigned same = (lane > 0 && v[0] == vl) ? 1u : 0u;
 #pragma unroll
-      for (int j = 0; j < PX; ++j)
-        if (j == e) l = v[j];
-      if (l == 0) continue;
-      if (l < 0 || l > nb) {
-        raise_flag(status, FLAG_BAD_LABEL);
-        continue;
+      for (int j = 1; j < PX; ++j) same |= (v[j] == v[j - 1] ? 1u : 0u) << j;
+      unsigned starts = vmask & ~same;
+      // the row's labels and run starts in shared memory, the runs listed in order
+      *reinterpret_cast<int4*>(rb + xl) = make_int4(v[0], v[1], v[2], v[3]);
+      *reinterpret_cast<int4*>(rb + xl + 4) = make_int4(v[4], v[5], v[6], v[7]);
+      const int ns = __popc(starts);
+      int inc = ns;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const int t = __shfl_up_sync(FULL, inc, d);
+        if (lane >= d) inc += t;
       }
-      unsigned xs = (unsigned)(xl + sj), xe = (unsigned)(xl + e);   // columns in the area
-      unsigned area = xe - xs + 1u;
-      unsigned sxs = (xs + xe) * area / 2u;
-      unsigned edge = (edgeRow || (xs == 0u && edgeL) || (x0 + (int)xe == x1 && edgeR)) ? 1u : 0u;
-      if (ends == 0u && contNext) {   // my last run goes on into the next lanes
-        area += cl;
-        sxs += cx;
-        xe = max(xe, cm);
-        edge |= ce;
+      const int nrun = __shfl_sync(FULL, inc, 31);
+      int pos = inc - ns;
+      while (starts) {
+        const int j = __ffs(starts) - 1;
+        starts &= starts - 1;
+        L[pos++] = (uint16_t)(xl + j);
       }
-      const int first = y * g.W + x0 + (int)xs;
-      unsigned h = ((unsigned)l * 2654435761u) >> (32 - STATS_HASH_BITS);
-      bool kept = false;
-      for (int probe = 0; probe < 16 && !kept; ++probe) {
-        const int prev = atomicCAS(&hkey[h], 0, l);
-        if (prev == 0 || prev == l) {
-          atomicAdd(&harea[h], (int)area);
-          if (edge) atomicOr(&harea[h], EDGE_BIT);
-          atomicMin(&hxmin[h], (int)xs);
-          atomicMax(&hxmax[h], (int)xe);
-          atomicMax(&hymax[h], y);
-          atomicMin(&hfirst[h], first);
-          atomicAdd(&hsy[h], (unsigned)(y - y0) * area);
-          atomicAdd(&hsx[h], sxs);
-          kept = true;
+      if (lane == 0) L[nrun] = (uint16_t)aw;   // the end of the last run
+      __syncwarp();
+      const bool edgeRow = (y == y0 && topIn) || (y == y1 && botIn);
+      for (int k = lane; k < nrun; k += 32) {
+        const int l = rb[L[k]];
+        if (l == 0) continue;
+        if (l < 0 || l > nb) {
+          raise_flag(status, FLAG_BAD_LABEL);
+          continue;
         }
-        h = (h + 1) & (STATS_HASH - 1);
+        const int xs = ax0 + L[k], xe = ax0 + L[k + 1] - 1;   // columns in the strip
+        const unsigned n = (unsigned)(xe - xs + 1);
+        const unsigned long long sxs = (unsigned long long)((unsigned)(xs + xe) * n / 2u);
+        const unsigned long long add = ((unsigned long long)n << ACC_N) |
+                                       ((unsigned long long)((unsigned)(y - y0) * n) << ACC_Y) | sxs;
+        const bool eA = edgeRow || (xs == ax0 && areaL) || (xe == ax0 + aw - 1 && areaR);
+        const bool eS = edgeRow || (xs == 0 && stripL) || (xe == sw - 1 && stripR);
+        const uint8_t edge = (eA ? EDGE_AREA : 0) | (eS ? EDGE_STRIP : 0);
+        const int firstRel = ((y - y0) << FIRST_ROW_SHIFT) | xs;
+        if (!table_add(ta, l, add, xs, xe, y, firstRel, edge)) {
+          spilled = 1;
+          const long long ge = base + l - 1;   // the table is crowded: straight to the global entry
+          if (ge < capacity) partial_to_global(stats + ge, add, xs, xe, y, firstRel, y0, x0, g);
+        }
       }
-      if (!kept) {   // the table is crowded: straight to the global entry
+      __syncwarp();
+    }
+    __syncthreads();
+    // the area's labels: wholly inside it -> stored; else into the strip's table
+    if (threadIdx.x < STATS_HASH) {
+      const int i = threadIdx.x, l = ta.key[i];
+      if (l != 0) {
         const long long ge = base + l - 1;
-        if (ge < capacity)
-          stats_add_global(stats + ge, (int)area, y, x0 + (int)xs, y, x0 + (int)xe, first,
-                           (unsigned long long)y * area,
-                           (unsigned long long)sxs + (unsigned long long)x0 * area);
+        if (ge < capacity) {
+          if (!(ta.edge[i] & EDGE_AREA))
+            partial_store(stats + ge, ta.acc[i], ta.xmin[i], ta.xmax[i], ta.ymax[i], ta.first[i], y0, x0, g);
+          else if (!table_add(ts, l, ta.acc[i], ta.xmin[i], ta.xmax[i], ta.ymax[i], ta.first[i],
+                              ta.edge[i] & EDGE_STRIP)) {
+            spilled = 1;
+            partial_to_global(stats + ge, ta.acc[i], ta.xmin[i], ta.xmax[i], ta.ymax[i], ta.first[i], y0, x0, g);
+          }
+        }
+        table_clear(ta, i);
       }
     }
+    __syncthreads();
   }
+  // the strip's labels: wholly inside it (and no partial spilled) -> stored;
+  // else added to the global entry
   __syncthreads();
-  for (int i = threadIdx.x; i < STATS_HASH; i += STATS_NT) {
-    const int l = hkey[i];
-    if (l == 0) continue;
-    const long long ge = base + l - 1;
-    if (ge >= capacity) continue;
-    const int area = harea[i] & (EDGE_BIT - 1);
-    const int first = hfirst[i];
-    const int ymin = div_w(first, g);
-    const unsigned long long sy = (unsigned long long)hsy[i] + (unsigned long long)y0 * area;
-    const unsigned long long sx = (unsigned long long)hsx[i] + (unsigned long long)x0 * area;
-    if (harea[i] & EDGE_BIT) {
-      stats_add_global(stats + ge, area, ymin, x0 + hxmin[i], hymax[i], x0 + hxmax[i], first, sy, sx);
-    } else {   // wholly inside this area: this block is the entry's only writer
-      ccl_region_stat r;
-      r.area = area;
-      r.y_min = ymin;
-      r.x_min = x0 + hxmin[i];
-      r.y_max = hymax[i];
-      r.x_max = x0 + hxmax[i];
-      r.first = first;
-      r.sum_y = (int64_t)sy;
-      r.sum_x = (int64_t)sx;
-      stats[ge] = r;
+  if (threadIdx.x < STATS_HASH) {
+    const int i = threadIdx.x, l = ts.key[i];
+    if (l != 0) {
+      const long long ge = base + l - 1;
+      if (ge < capacity) {
+        if ((ts.edge[i] & EDGE_STRIP) || spilled)
+          partial_to_global(stats + ge, ts.acc[i], ts.xmin[i], ts.xmax[i], ts.ymax[i], ts.first[i], y0, x0, g);
+        else
+          partial_store(stats + ge, ts.acc[i], ts.xmin[i], ts.xmax[i], ts.ymax[i], ts.first[i], y0, x0, g);
+      }
     }
   }
 }
