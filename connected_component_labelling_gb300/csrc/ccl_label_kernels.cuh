@@ -730,11 +730,12 @@ __device__ __forceinline__ long long parked_label_index(const TileCoord& t, cons
 
 // Collapse + Number for the border leaders linked across seams (a warp per
 // tile, a lane per slot): each walks to its region's root and parks the
-// root's label for its slot.  After k_seams the entries only change here,
-// and only a root's own: the first walker to reach a root stores the root's
-// label in the entry's upper half (top bit set, in place of the key), so
-// that the other walkers that reach it read the label with the entry.
-constexpr unsigned long long LABELLED = 1ull << 63;
+// root's label for its slot.  After k_seams an entry changes only here, and
+// only to carry its region's label: label << 32 | LABEL_MARK (no slot has
+// that id: an image has fewer than 2^32 - 1 slots).  The first walker to
+// reach a root labels the root, and every walker labels the slot it started
+// from, so that later walks stop at the first labelled entry they meet.
+constexpr uint32_t LABEL_MARK = 0xFFFFFFFFu;
 
 __global__ void __launch_bounds__(32 * RESOLVE_WARPS) k_resolve(Work wk, int32_t* labels, Geom g,
                                                                 long long nTiles, int cap, int* status) {
@@ -749,15 +750,16 @@ __global__ void __launch_bounds__(32 * RESOLVE_WARPS) k_resolve(Work wk, int32_t
   for (int k = lane; k < count; k += 32) {
     const uint32_t s = s0 + k;
     unsigned long long v = ld_relaxed_gpu(Pi + s);
-    if ((uint32_t)v == s) continue;   // still a leader: k_number labels it
+    // still a leader (maybe labelled by a walker already): k_number labels it
+    if ((uint32_t)v == s || (uint32_t)v == LABEL_MARK) continue;
     CCL_COUNT(CCL_CNT_RESOLVE_STEPS);
     const int q = wk.bls[tile * g.SL + k] & 0xFFF;
     uint32_t x = (uint32_t)v;
     int st = 0;
-    for (; st < cap; ++st) {   // to the root (the entries are pointers: no halving here)
+    for (; st < cap; ++st) {   // to the root, or to a node already labelled
       if (x >= n) break;
       v = ld_relaxed_gpu(Pi + x);
-      if ((uint32_t)v == x) break;
+      if ((uint32_t)v == LABEL_MARK || (uint32_t)v == x) break;
       x = (uint32_t)v;
     }
     if (st == cap || x >= n) {
@@ -765,12 +767,14 @@ __global__ void __launch_bounds__(32 * RESOLVE_WARPS) k_resolve(Work wk, int32_t
       continue;
     }
     int lab;
-    if (v & LABELLED) {
-      lab = (int)((v >> 32) & 0x7FFFFFFFu);
+    if ((uint32_t)v == LABEL_MARK) {
+      lab = (int)(v >> 32);
     } else {
       lab = label_of_root(wk, x, t.b, g, status);
-      atomicCAS(Pi + x, v, LABELLED | ((unsigned long long)((uint32_t)lab & 0x7FFFFFFFu) << 32) | x);
+      atomicCAS(Pi + x, v, ((unsigned long long)(uint32_t)lab << 32) | LABEL_MARK);
     }
+    // this slot carries the label from now on: later walks through it stop here
+    atomicExch(Pi + s, ((unsigned long long)(uint32_t)lab << 32) | LABEL_MARK);
     labels[parked_label_index(t, g, q)] = lab;
   }
 }
