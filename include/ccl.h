@@ -29,16 +29,24 @@
  *    packed 32-bit copy of the picture was slower and twice the memory).
  *  - Pixel equality compares all pixel_bytes bytes (RGBA: alpha included).
  *  - Labels are canonical per image: numbering restarts at 1 in every image.
- *  - H*W must be below 2^31 (CCL_ERR_TOO_LARGE otherwise); batch*H*W may
- *    exceed it.
+ *  - H*W must be below 2^32 (CCL_ERR_TOO_LARGE otherwise; "every-colour"
+ *    ch. 11 names images of more than 2^31 pixels as the case it never ran):
+ *    raster indices inside an image are 32-bit.  Also refused: an image whose
+ *    256 x 16 tiles would hold 2^32 or more border slots (only images of one
+ *    or two rows close to that size), and a grid of 2^31 or more tiles.
+ *    batch*H*W may exceed 2^32.  Labels stay int32: an image with more than
+ *    2^31 - 1 regions completes with its counts clamped and the device status
+ *    CCL_ERR_TOO_LARGE (ccl_last_status).
  *  - batch == 0, H == 0 or W == 0 is a valid empty call (n_regions_out, if
  *    given, is set to 0 for every image).
  *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL is the legacy
  *    default stream).  The return value reports argument and launch errors
  *    only; a device-side limit that trips is reported by ccl_last_status().
- *  - `labels_i32` doubles as the union-find parent array while the call
- *    runs ("every-colour", ch. 09: the labels are the only per-pixel memory),
- *    so it must not overlap `img`.
+ *  - `labels_i32` also holds, between two stages of the call, the labels of
+ *    regions joined across tile seams (parked inside their tile until the
+ *    last stage reads them back), so it must not overlap `img`; the counts
+ *    are written before the labels, so `n_regions_out` must not overlap
+ *    `labels_i32` either.
  *  - All pointers are owned by the caller; the library frees nothing of theirs.
  */
 #ifndef CCL_H_
@@ -57,7 +65,8 @@ typedef struct CUstream_st* ccl_stream_t;
 typedef enum {
   CCL_OK = 0,
   CCL_ERR_INVALID_ARG = 1,   /* bad pointer, size, enum value or alignment */
-  CCL_ERR_TOO_LARGE = 2,     /* H*W >= 2^31 */
+  CCL_ERR_TOO_LARGE = 2,     /* H*W >= 2^32 (see the conventions); on the device:
+                                more regions than int32 labels hold */
   CCL_ERR_CUDA = 3,          /* a CUDA runtime call or launch failed */
   CCL_ERR_NO_MEMORY = 4,     /* workspace allocation failed / too small */
   CCL_ERR_DEVICE_LIMIT = 5   /* a bounded device loop reached its cap */
@@ -74,7 +83,7 @@ enum { CCL_MODE_ALL = 0, CCL_MODE_BINARY = 1 };
  *   labels_i32     device pointer, batch*H*W int32, written completely
  *   n_regions_out  device pointer to batch int32 (region count per image),
  *                  or NULL
- * Scratch (ccl_workspace_bytes(...) bytes, about 2.5 bytes per pixel) comes
+ * Scratch (ccl_workspace_bytes(...) bytes, about 3.9 bytes per pixel) comes
  * from a stream-ordered memory pool the library keeps per device.
  * Returns CCL_OK or an error status; nothing is written on an argument error.
  */
@@ -83,10 +92,14 @@ int ccl_label(const void* img, int batch, int H, int W, int pixel_bytes,
               int32_t* n_regions_out, ccl_stream_t stream);
 
 /* Bytes of device workspace ccl_label_ws needs for these arguments
- * (0 for an empty call or invalid arguments): about 2.15 bytes per pixel
- * plus 1348 bytes per tile of 256 columns x 16 rows -- about 2.5 bytes per
- * pixel in all for images of many whole tiles; a single row of 2^31 - 1
- * pixels, whose tiles hold one row each, needs about 7.4 bytes per pixel. */
+ * (0 for an empty call or invalid arguments).  Per image row a run-start bit
+ * per pixel (and, in binary mode, a foreground bit); per tile of 256 columns
+ * x 16 rows a leader for every run it can hold, its leader bits, run bases,
+ * seam joins, and for every border pixel a slot record and an 8-byte parent
+ * entry; chunk counts for the numbering.  About 3.9 bytes per pixel for
+ * images of many whole tiles (4.0 in binary mode); thin images cost more per
+ * pixel, since every pixel of a one-row tile is a border pixel (one row of
+ * 2^31 - 1 pixels: about 15 bytes per pixel). */
 size_t ccl_workspace_bytes(int batch, int H, int W, int pixel_bytes,
                            int connectivity, int mode);
 
@@ -111,8 +124,9 @@ int ccl_label_ws(const void* img, int batch, int H, int W, int pixel_bytes,
  * label 0 in Start and take part in nothing after).  ignore_value 0 is the
  * same as CCL_MODE_BINARY.  The other pixels are labelled as in
  * CCL_MODE_ALL: 1..n by first pixel in raster order.
- * `workspace` as in ccl_label_ws (ccl_workspace_bytes bytes, 256-byte
- * aligned), or NULL to take scratch from the library's per-device pool.
+ * `workspace` as in ccl_label_ws, sized by ccl_workspace_bytes(..., 
+ * CCL_MODE_BINARY) (the ignoring pipeline keeps foreground bits), 256-byte
+ * aligned; or NULL to take scratch from the library's per-device pool.
  * Returns CCL_ERR_INVALID_ARG if ignore_value does not fit in pixel_bytes.
  */
 int ccl_label_ignore(const void* img, int batch, int H, int W,
@@ -129,8 +143,11 @@ int ccl_label_ignore(const void* img, int batch, int H, int W,
  * the library's, overlapped with the kernels (a band is labelled inside its
  * tiles while the next is copied in; a band's labels are copied out once
  * numbered).  Device buffers come from the library's pool.  Returns after the
- * results are in host memory (the stream is synchronised); a tripped device
- * limit is returned directly as CCL_ERR_DEVICE_LIMIT.
+ * results are in host memory (the stream is synchronised); a device-side
+ * finding of this call (a tripped limit: CCL_ERR_DEVICE_LIMIT; more regions
+ * than int32 labels: CCL_ERR_TOO_LARGE) is returned directly.  The call keeps
+ * a status word of its own: findings of other calls stay in the device's word
+ * for ccl_last_status, and this call's do not go there.
  */
 int ccl_label_host(const void* img_host, int batch, int H, int W,
                    int pixel_bytes, int connectivity, int mode,
@@ -141,9 +158,11 @@ int ccl_label_host(const void* img_host, int batch, int H, int W,
  * ccl_last_status -- synchronises `stream`, then returns and clears the
  * current device's sticky device-side status: CCL_ERR_DEVICE_LIMIT if a
  * bounded loop (a union-find walk or a union retry) reached its cap in any
- * call since the last check, CCL_ERR_NO_MEMORY / CCL_ERR_INVALID_ARG for the
+ * call since the last check, CCL_ERR_TOO_LARGE if an image had more regions
+ * than int32 labels hold, CCL_ERR_NO_MEMORY / CCL_ERR_INVALID_ARG for the
  * device-side findings of ccl_region_stats (see there), CCL_ERR_CUDA if the
- * stream reports an error, else CCL_OK.  The caps are far above any
+ * stream reports an error, else CCL_OK.  Every labelling call except
+ * ccl_label_host and ccl_label_noalloc reports into this word.  The caps are far above any
  * legitimate walk; tripping one means the labels of that call are not valid.
  */
 int ccl_last_status(ccl_stream_t stream);
@@ -195,8 +214,8 @@ long long ccl_kernel_launches(void);
  * held by every GPU that loads the library until the process exits; 256
  * bytes of it are a status word and the rest must be at least
  * ccl_workspace_bytes(...) for these arguments, else the call returns
- * CCL_ERR_TOO_LARGE without doing anything (about 2.5 bytes per pixel:
- * roughly 13 million pixels per call).
+ * CCL_ERR_TOO_LARGE without doing anything (about 3.9 bytes per pixel:
+ * roughly 8.5 million pixels per call).
  *  - The first call on a device looks up the array's device address (with
  *    that device current) and caches it; make that first call before any
  *    stream capture.
@@ -252,7 +271,8 @@ size_t ccl_region_stats_workspace_bytes(int batch);
  * bytes, 256-byte aligned, or NULL to take it from the library's pool.  All
  * buffers are the caller's; the call only reads labels_i32 and n_regions.
  * Asynchronous on `stream`.  Host-side errors are returned (bad pointer,
- * alignment or size: CCL_ERR_INVALID_ARG; H*W >= 2^31: CCL_ERR_TOO_LARGE;
+ * alignment or size: CCL_ERR_INVALID_ARG; H*W >= 2^31, whose raster indices
+ * the int32 `first` field cannot hold: CCL_ERR_TOO_LARGE;
  * workspace too small: CCL_ERR_NO_MEMORY).  Device-side findings go to
  * ccl_last_status: CCL_ERR_NO_MEMORY if the regions outnumber `capacity`
  * (entries at and beyond it are skipped), CCL_ERR_INVALID_ARG if a label lies
