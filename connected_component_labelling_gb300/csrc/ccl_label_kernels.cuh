@@ -421,50 +421,47 @@ __global__ void __launch_bounds__(NT, 8) k_tile_local(const T* __restrict__ img,
   __syncthreads();
 
   // ---- Collapse: every run points straight at its tile-local leader; the
-  // leaders are the runs that are their own leader.  The leaders of regions
-  // that touch the tile border are marked.
+  // leaders are the runs that are their own leader.  The first run on the
+  // tile border to reach a leader marks it and gives it a slot: a parent
+  // entry that names itself, with its key, the raster position of its first
+  // pixel (its run's rank in the row stands for the column: ranks keep the
+  // order, and x0 + rank < x0 + width, the next tile's first column), and
+  // its run and row.
+  uint16_t* slotOf = &jl[0][0];   // TILE entries
   const int rbFirst = rbS[1], rbLast = rbS[t.th - 1];   // runs of the first row: [0, rbFirst)
   for (int base = warp * 32; base < total; base += NT) {   // warp-uniform bounds
     const int q = base + lane;
     const bool v = q < total;
     int root = -1;
+    bool fresh = false;   // the first border run of its leader
     if (v) {
       root = find_s(par, q, cap, status);
       st_relaxed_cta(par + q, root);
       wk.ent[tile * g.ENT + q] = (uint16_t)root;
-      if (q < rbFirst || q >= rbLast || ((bcol[q >> 5] >> (q & 31)) & 1u))
-        atomicOr(&bmark[root >> 5], 1u << (root & 31));
+      if (q < rbFirst || q >= rbLast || ((bcol[q >> 5] >> (q & 31)) & 1u)) {
+        const unsigned bit = 1u << (root & 31);
+        fresh = !(atomicOr(&bmark[root >> 5], bit) & bit);
+      }
     }
     const unsigned bal = __ballot_sync(FULL, v && root == q);
     if (lane == 0) {
       lrs[base >> 5] = bal;
       wk.lr[tile * g.LRT + (base >> 5)] = bal;
     }
-  }
-  __syncthreads();
-
-  // ---- a slot for every marked leader: its parent entry names itself, with
-  // its key, the raster position of its first pixel (its run's rank in the
-  // row stands for the column: ranks keep the order, and x0 + rank < x0 +
-  // width, the next tile's first column), and its run and row
-  uint16_t* slotOf = &jl[0][0];   // TILE entries
-  for (int base = warp * 32; base < total; base += NT) {   // warp-uniform bounds
-    const int q = base + lane;
-    const bool mk = q < total && ((bmark[q >> 5] >> (q & 31)) & 1u);
-    const unsigned bal = __ballot_sync(FULL, mk);
-    if (bal) {   // warp-uniform
+    const unsigned fb = __ballot_sync(FULL, fresh);
+    if (fb) {   // warp-uniform
       int k0 = 0;
-      if (lane == 0) k0 = atomicAdd(&nb, __popc(bal));
+      if (lane == 0) k0 = atomicAdd(&nb, __popc(fb));
       k0 = __shfl_sync(FULL, k0, 0);
-      if (mk) {
-        const int k = k0 + __popc(bal & ((1u << lane) - 1u));
-        const int r = row_of_run(rbS, q);
+      if (fresh) {
+        const int k = k0 + __popc(fb & ((1u << lane) - 1u));
+        const int r = row_of_run(rbS, root);
         const long long gi = tile * g.SL + k;   // entry index; the slot's id in its image:
         const uint32_t sid = (uint32_t)(gi - (long long)t.b * g.slotsPerImage);
-        const uint32_t key = (uint32_t)((long long)(t.y0 + r) * g.W + t.x0 + (q - rbS[r]));
+        const uint32_t key = (uint32_t)((long long)(t.y0 + r) * g.W + t.x0 + (root - rbS[r]));
         wk.P[gi] = ((unsigned long long)key << 32) | sid;
-        wk.bls[gi] = (uint16_t)(q | (r << 12));
-        slotOf[q] = (uint16_t)k;
+        wk.bls[gi] = (uint16_t)(root | (r << 12));
+        slotOf[root] = (uint16_t)k;
       }
     }
   }
