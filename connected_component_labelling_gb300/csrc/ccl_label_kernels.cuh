@@ -790,7 +790,7 @@ __global__ void __launch_bounds__(NT, 8) k_number(Work wk, int32_t* labels, Geom
   __shared__ uint32_t lrS[LRW];
   __shared__ int rbS[TH + 1];
   __shared__ uint32_t offS[TH];
-  constexpr int PRE = 4;   // runs a thread prefetches the leader of
+  constexpr int PRE = 3;   // runs a thread prefetches the leader of
   const long long tile = tile0 + blockIdx.x;   // launches may cover a band of tiles
   const TileCoord t = tile_coord_of(g, tile);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, xl = lane * PX;
