@@ -361,9 +361,9 @@ void launch_resolve(const Pipe& q) {
 // Number for tiles [tile0, tile0 + ntiles)
 void launch_number(const Pipe& q, long long tile0, long long ntiles) {
   if (q.mode == CCL_MODE_BINARY)
-    k_number<true><<<(unsigned)ntiles, NT, 0, q.st>>>(q.wk, q.labels, q.g, q.status, tile0);
+    k_number<true><<<(unsigned)ntiles, NUM_NT, 0, q.st>>>(q.wk, q.labels, q.g, q.status, tile0);
   else
-    k_number<false><<<(unsigned)ntiles, NT, 0, q.st>>>(q.wk, q.labels, q.g, q.status, tile0);
+    k_number<false><<<(unsigned)ntiles, NUM_NT, 0, q.st>>>(q.wk, q.labels, q.g, q.status, tile0);
 }
 
 // The whole labelling pipeline on `st`; `events` whether the optional

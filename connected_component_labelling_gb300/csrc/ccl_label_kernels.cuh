@@ -780,9 +780,14 @@ __global__ void __launch_bounds__(32 * RESOLVE_WARPS) k_resolve(Work wk, int32_t
 // order (chunk offset + rank among the chunk's leaders), leaders linked
 // across a seam the label k_resolve found; every run takes its leader's
 // label and every pixel its run's.
+// Number is bound by the latency of each tile's records (loads, then three
+// barriers), so its blocks are small: four warps, four rows each, and about
+// eleven tiles in flight on an SM (shared memory is the limit).
+constexpr int NUM_NT = 128;   // threads of a Number block
+
 template <bool BIN>
-__global__ void __launch_bounds__(NT, 8) k_number(Work wk, int32_t* labels, Geom g, int* status,
-                                               long long tile0) {
+__global__ void __launch_bounds__(NUM_NT, NUM_NT == 256 ? 8 : 12) k_number(Work wk, int32_t* labels, Geom g,
+                                                                     int* status, long long tile0) {
   __shared__ __align__(16) int runLab[TILE];
   __shared__ uint32_t swS[TH][WPT];
   __shared__ uint32_t fwS[BIN ? TH : 1][WPT];
@@ -790,7 +795,8 @@ __global__ void __launch_bounds__(NT, 8) k_number(Work wk, int32_t* labels, Geom
   __shared__ uint32_t lrS[LRW];
   __shared__ int rbS[TH + 1];
   __shared__ uint32_t offS[TH];
-  constexpr int PRE = 3;   // runs a thread prefetches the leader of
+  constexpr int NTN = NUM_NT, RPWN = TH / (NTN / 32);   // rows a warp writes
+  constexpr int PRE = 768 / NTN;   // runs a thread prefetches the leader of
   const long long tile = tile0 + blockIdx.x;   // launches may cover a band of tiles
   const TileCoord t = tile_coord_of(g, tile);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, xl = lane * PX;
@@ -798,13 +804,13 @@ __global__ void __launch_bounds__(NT, 8) k_number(Work wk, int32_t* labels, Geom
   const uint16_t* ent = wk.ent + tile * g.ENT;
   // every load of the tile's records is issued before the first barrier
   // (entries past the tile's runs are read but never used): the leaders of
-  // the first PRE * NT runs, and the leader-bit words holding those runs
+  // the first PRE * NTN runs, and the leader-bit words holding those runs
   const int total = __ldg(wk.hdr + tile * TH + TH - 1);
   int pe[PRE];
   uint32_t pl[PRE];
 #pragma unroll
   for (int i = 0; i < PRE; ++i) {
-    const int q = tid + i * NT;
+    const int q = tid + i * NTN;
     pe[i] = q < g.ENT ? __ldg(ent + q) : 0;
     pl[i] = q < g.ENT ? __ldg(wk.lr + tile * g.LRT + (q >> 5)) : 0u;
   }
@@ -826,8 +832,12 @@ __global__ void __launch_bounds__(NT, 8) k_number(Work wk, int32_t* labels, Geom
     swS[r][m] = w;
     spS[r][m] = inc - pc;
     if (BIN) fwS[r][m] = f;
-  } else {
-    const int i = tid - TH * WPT;
+  }
+  // the leader-bit words, run bases and chunk offsets: a thread each (the
+  // threads past the rows' words, or all of a block of TH * WPT threads)
+  static_assert(NTN == TH * WPT || NTN == 2 * TH * WPT, "loaders of the tile's records");
+  if (NTN == TH * WPT || tid >= TH * WPT) {
+    const int i = NTN == TH * WPT ? tid : tid - TH * WPT;
     if (i < g.LRT) lrS[i] = __ldg(wk.lr + tile * g.LRT + i);
     if (i < TH) rbS[i + 1] = __ldg(wk.hdr + tile * TH + i);
     if (i == TH) rbS[0] = 0;
@@ -841,18 +851,18 @@ __global__ void __launch_bounds__(NT, 8) k_number(Work wk, int32_t* labels, Geom
   // the label k_resolve parked in the tile
 #pragma unroll
   for (int i = 0; i < PRE; ++i) {
-    const int q = tid + i * NT;
+    const int q = tid + i * NTN;
     if (q < total && pe[i] == q && !((pl[i] >> (q & 31)) & 1u)) runLab[q] = labels[parked_label_index(t, g, q)];
   }
-  for (int q = tid + PRE * NT; q < total; q += NT)
+  for (int q = tid + PRE * NTN; q < total; q += NTN)
     if (__ldg(ent + q) == q && !((__ldg(wk.lr + tile * g.LRT + (q >> 5)) >> (q & 31)) & 1u))
       runLab[q] = labels[parked_label_index(t, g, q)];
   __syncthreads();
   // the leaders still in the leader bits, row by row (a warp per row of its
   // own): 1 + the chunk's offset + the leaders before them in the row
 #pragma unroll
-  for (int k = 0; k < RPW; ++k) {
-    const int r = warp * RPW + k;
+  for (int k = 0; k < RPWN; ++k) {
+    const int r = warp * RPWN + k;
     if (r >= t.th) continue;   // warp-uniform
     const int re = rbS[r + 1];
     uint32_t lab = offS[r] + 1u;
@@ -873,10 +883,10 @@ __global__ void __launch_bounds__(NT, 8) k_number(Work wk, int32_t* labels, Geom
   // the label read back above)
 #pragma unroll
   for (int i = 0; i < PRE; ++i) {
-    const int q = tid + i * NT;
+    const int q = tid + i * NTN;
     if (q < total && pe[i] != q) runLab[q] = runLab[pe[i]];
   }
-  for (int q = tid + PRE * NT; q < total; q += NT) {
+  for (int q = tid + PRE * NTN; q < total; q += NTN) {
     const int e = __ldg(ent + q);
     if (e != q) runLab[q] = runLab[e];
   }
@@ -884,8 +894,8 @@ __global__ void __launch_bounds__(NT, 8) k_number(Work wk, int32_t* labels, Geom
   const int nval = max(0, min(PX, t.tw - xl));
   const bool vec = g.vec_out && nval == PX;
 #pragma unroll
-  for (int k = 0; k < RPW; ++k) {
-    const int r = warp * RPW + k;
+  for (int k = 0; k < RPWN; ++k) {
+    const int r = warp * RPWN + k;
     if (r >= t.th) continue;
     const int m = lane >> 2, sh = 8 * (lane & 3);
     const uint32_t w = swS[r][m];
