@@ -715,7 +715,8 @@ __device__ __forceinline__ int label_of_root(const Work& wk, uint32_t s, int b, 
   return (int)lab;
 }
 
-constexpr int RESOLVE_WARPS = 2;   // tiles (a warp each) per block: small blocks free their slot sooner
+constexpr int RESOLVE_WARPS = 2;   // tiles (a warp each) per block: small blocks free their slot sooner;
+                                   // held to 32 registers so that 32 blocks (64 warps) fit an SM
 
 // The label found for a leader linked across a seam (run q of its tile)
 // waits in the labels buffer, inside that tile (q < the tile's pixels), until
@@ -734,7 +735,7 @@ __device__ __forceinline__ long long parked_label_index(const TileCoord& t, cons
 // from, so that later walks stop at the first labelled entry they meet.
 constexpr uint32_t LABEL_MARK = 0xFFFFFFFFu;
 
-__global__ void __launch_bounds__(32 * RESOLVE_WARPS) k_resolve(Work wk, int32_t* labels, Geom g,
+__global__ void __launch_bounds__(32 * RESOLVE_WARPS, 32) k_resolve(Work wk, int32_t* labels, Geom g,
                                                                 long long nTiles, int cap, int* status) {
   const long long tile = (long long)blockIdx.x * RESOLVE_WARPS + (threadIdx.x >> 5);
   if (tile >= nTiles) return;
