@@ -304,7 +304,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ccl", choices=["ccl", "reference"])
     ap.add_argument("--workload", default="c4")
-    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--e2e-steps", type=int, default=8)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-stats", action="store_true",
@@ -539,9 +539,12 @@ def main():
         floor_ms = statistics.median(up_ms) + statistics.median(down_ms)
         barrier(world)
         t0 = time.perf_counter()
+        call_ms = []   # each call returns after its own synchronisation
         for _ in range(args.e2e_steps):
+            tc = time.perf_counter()
             rc = ccl.ccl_label_host(himg.data_ptr(), B, H, W, pb, conn, mode, hlab.data_ptr(),
                                     hn.data_ptr(), sp)
+            call_ms.append((time.perf_counter() - tc) * 1e3)
             if rc != ccl.CCL_OK:
                 raise ccl.CCLError(rc, "ccl_label_host")
         dt = (time.perf_counter() - t0) / args.e2e_steps
@@ -551,11 +554,14 @@ def main():
                "h2d_bytes_per_step": px * pb, "d2h_bytes_per_step": px * 4 + B * 4,
                "steps": args.e2e_steps, "api": "ccl_label_host (pinned host buffers)",
                "labels_match_device_run": same,
+               "ms_per_call_median": statistics.median(call_ms), "ms_per_call_min": min(call_ms),
+               "ms_per_call_max": max(call_ms),
                "copy_floor_ms": floor_ms, "h2d_ms": statistics.median(up_ms),
                "d2h_ms": statistics.median(down_ms), "frac_of_floor": floor_ms / (dt * 1e3),
                "floor_note": "the same pinned buffers copied alone in this process (image up, "
                              "then labels down, median of the e2e steps); frac_of_floor = "
-                             "copy_floor_ms / ms_per_step"}
+                             "copy_floor_ms / ms_per_step; ms_per_call_* are single calls "
+                             "(the host side is shared: a call can stall on it)"}
         del himg, hlab
 
     # ---- cpu baseline and parity: the oracle over the whole workload on this
