@@ -555,7 +555,7 @@ def main():
                "steps": args.e2e_steps, "api": "ccl_label_host (pinned host buffers)",
                "labels_match_device_run": same,
                "ms_per_call_median": statistics.median(call_ms), "ms_per_call_min": min(call_ms),
-               "ms_per_call_max": max(call_ms),
+               "ms_per_call_max": max(call_ms), "ms_per_call": [round(c, 3) for c in call_ms],
                "copy_floor_ms": floor_ms, "h2d_ms": statistics.median(up_ms),
                "d2h_ms": statistics.median(down_ms), "frac_of_floor": floor_ms / (dt * 1e3),
                "floor_note": "the same pinned buffers copied alone in this process (image up, "
