@@ -89,7 +89,9 @@ __device__ __forceinline__ void stats_add_global(ccl_region_stat* e, int area, i
 }
 
 // A block per strip of SSEG areas of 256 columns x SR rows, taken one area
-// after another.  A warp takes one row of the area at a time, a lane 8
+// after another.  Blocks are small (four warps) and strips short, so that
+// many strips are in flight on an SM: the kernel waits on its shared-memory
+// chains more than it issues.  A warp takes one row of the area at a time, a lane 8
 // consecutive labels (as in k_tile_local).  The row's runs of equal label
 // (run starts from equal-to-left masks) are listed in shared memory and dealt
 // out to the warp's lanes, a run each, so that busy rows keep every lane
@@ -110,8 +112,8 @@ __device__ __forceinline__ void stats_add_global(ccl_region_stat* e, int area, i
 #ifndef CCL_STATS_HASH
 #define CCL_STATS_HASH 256
 #define CCL_STATS_ROWS 16
-#define CCL_STATS_SEGS 8
-#define CCL_STATS_NT 256
+#define CCL_STATS_SEGS 4
+#define CCL_STATS_NT 128
 #endif
 constexpr int STATS_HASH = CCL_STATS_HASH;
 constexpr int SR = CCL_STATS_ROWS;       // rows of a statistics area
@@ -122,7 +124,6 @@ constexpr int STATS_NWARPS = STATS_NT / 32;
 constexpr int STATS_HASH_BITS = STATS_HASH == 1024 ? 10 : STATS_HASH == 512 ? 9 : 8;
 static_assert((1 << STATS_HASH_BITS) == STATS_HASH, "a power of two");
 static_assert(STRIP_W <= 2048 && SR <= 16, "strip columns fit 11 bits, rows 4, in the packed first pixel");
-static_assert(STATS_HASH <= STATS_NT, "a thread per slot when an area's table is emptied");
 // the packed sums of a table slot: column sum (bits 0..25), row sum (26..45),
 // pixel count (46..63), all relative to the strip's corner.  A strip's pixels
 // keep each field below its top: sum of columns <= SR * STRIP_W^2 / 2 < 2^26,
@@ -193,7 +194,7 @@ __device__ __forceinline__ void partial_store(ccl_region_stat* e, unsigned long 
   *e = r;
 }
 
-__global__ void __launch_bounds__(STATS_NT, 6) k_region_stats(const int32_t* __restrict__ labels,
+__global__ void __launch_bounds__(STATS_NT, STATS_NT == 256 ? 6 : 12) k_region_stats(const int32_t* __restrict__ labels,
                                                      const int32_t* __restrict__ n_regions,
                                                      const long long* __restrict__ off,
                                                      ccl_region_stat* stats, long long capacity,
@@ -205,9 +206,9 @@ __global__ void __launch_bounds__(STATS_NT, 6) k_region_stats(const int32_t* __r
   // label of the strip's table may have global partials too, so none of that
   // table's entries is stored outright
   __shared__ int spilled;
-  if (threadIdx.x < STATS_HASH) {
-    table_clear(ta, threadIdx.x);
-    table_clear(ts, threadIdx.x);
+  for (int i = threadIdx.x; i < STATS_HASH; i += STATS_NT) {
+    table_clear(ta, i);
+    table_clear(ts, i);
   }
   if (threadIdx.x == 0) spilled = 0;
   __syncthreads();
@@ -297,8 +298,8 @@ __global__ void __launch_bounds__(STATS_NT, 6) k_region_stats(const int32_t* __r
     }
     __syncthreads();
     // the area's labels: wholly inside it -> stored; else into the strip's table
-    if (threadIdx.x < STATS_HASH) {
-      const int i = threadIdx.x, l = ta.key[i];
+    for (int i = threadIdx.x; i < STATS_HASH; i += STATS_NT) {
+      const int l = ta.key[i];
       if (l != 0) {
         const long long ge = base + l - 1;
         if (ge < capacity) {
@@ -318,8 +319,8 @@ __global__ void __launch_bounds__(STATS_NT, 6) k_region_stats(const int32_t* __r
   // the strip's labels: wholly inside it (and no partial spilled) -> stored;
   // else added to the global entry
   __syncthreads();
-  if (threadIdx.x < STATS_HASH) {
-    const int i = threadIdx.x, l = ts.key[i];
+  for (int i = threadIdx.x; i < STATS_HASH; i += STATS_NT) {
+    const int l = ts.key[i];
     if (l != 0) {
       const long long ge = base + l - 1;
       if (ge < capacity) {
