@@ -537,6 +537,7 @@ def main():
             down_ms.append(b.elapsed_time(c))
         del dimg
         floor_ms = statistics.median(up_ms) + statistics.median(down_ms)
+        floor_mean_ms = statistics.mean(up_ms) + statistics.mean(down_ms)
         barrier(world)
         t0 = time.perf_counter()
         call_ms = []   # each call returns after its own synchronisation
@@ -556,12 +557,15 @@ def main():
                "labels_match_device_run": same,
                "ms_per_call_median": statistics.median(call_ms), "ms_per_call_min": min(call_ms),
                "ms_per_call_max": max(call_ms), "ms_per_call": [round(c, 3) for c in call_ms],
-               "copy_floor_ms": floor_ms, "h2d_ms": statistics.median(up_ms),
+               "copy_floor_ms": floor_ms, "copy_floor_mean_ms": floor_mean_ms,
+               "frac_of_floor_median": floor_ms / statistics.median(call_ms),
+               "h2d_ms": statistics.median(up_ms),
                "d2h_ms": statistics.median(down_ms), "frac_of_floor": floor_ms / (dt * 1e3),
                "floor_note": "the same pinned buffers copied alone in this process (image up, "
                              "then labels down, median of the e2e steps); frac_of_floor = "
-                             "copy_floor_ms / ms_per_step; ms_per_call_* are single calls "
-                             "(the host side is shared: a call can stall on it)"}
+                             "copy_floor_ms / ms_per_step; frac_of_floor_median = copy_floor_ms / "
+                             "ms_per_call_median; copy_floor_mean_ms: the mean copies, which stall "
+                             "like the calls (the host side is shared)"}
         del himg, hlab
 
     # ---- cpu baseline and parity: the oracle over the whole workload on this
