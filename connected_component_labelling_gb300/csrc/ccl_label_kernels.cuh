@@ -782,8 +782,9 @@ __global__ void __launch_bounds__(32 * RESOLVE_WARPS, 32) k_resolve(Work wk, int
 // across a seam the label k_resolve found; every run takes its leader's
 // label and every pixel its run's.
 // Number is bound by the latency of each tile's records (loads, then three
-// barriers), so its blocks are small: four warps, four rows each, and about
-// eleven tiles in flight on an SM (shared memory is the limit).
+// barriers), so its blocks are small: four warps, four rows each, and twelve
+// tiles in flight on an SM (shared memory is the limit; eleven in the binary
+// mode, whose foreground bits take more).
 constexpr int NUM_NT = 128;   // threads of a Number block
 
 template <bool BIN>
@@ -859,8 +860,8 @@ __global__ void __launch_bounds__(NUM_NT, NUM_NT == 256 ? 8 : 12) k_number(Work 
     if (__ldg(ent + q) == q && !((__ldg(wk.lr + tile * g.LRT + (q >> 5)) >> (q & 31)) & 1u))
       runLab[q] = labels[parked_label_index(t, g, q)];
   __syncthreads();
-  // the leaders still in the leader bits, row by row (a warp per row of its
-  // own): 1 + the chunk's offset + the leaders before them in the row
+  // the leaders still in the leader bits, row by row (each row by one warp):
+  // 1 + the chunk's offset + the leaders before them in the row
 #pragma unroll
   for (int k = 0; k < RPWN; ++k) {
     const int r = warp * RPWN + k;
