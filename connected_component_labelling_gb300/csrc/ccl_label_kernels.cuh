@@ -520,6 +520,7 @@ __global__ void __launch_bounds__(32 * SEAM_WARPS) k_seams(Work wk, Geom g, long
   __shared__ __align__(16) uint16_t ownS[SEAM_WARPS][TW];        // slots of the first row
   __shared__ __align__(16) uint16_t abS[SEAM_WARPS][TW + 16];    // [8 + x]: slots of the row above
   __shared__ unsigned long long seenS[SEAM_WARPS][SEAM_HASH];
+  __shared__ uint16_t jlS[SEAM_WARPS][JCAP];                      // the top seam's joins
   constexpr unsigned long long EMPTY = ~0ull;
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31, xl = lane * PX;
   const long long tile = (long long)blockIdx.x * SEAM_WARPS + w;
@@ -564,12 +565,29 @@ __global__ void __launch_bounds__(32 * SEAM_WARPS) k_seams(Work wk, Geom g, long
       }
       if (lane == 0) abS[w][7] = t.tx > 0 ? wk.bsl[(ta - 1) * g.BSLW + g.BOFF + TW - 1] : NOSLOT;
       if (lane == 31) abS[w][8 + TW] = t.tx + 1 < g.tilesX ? wk.bsl[(ta + 1) * g.BSLW + g.BOFF] : NOSLOT;
-      __syncwarp();
+      // the joins listed (column | direction << 8) and dealt out to all
+      // lanes, as inside a tile: a lane's own joins would take as long as
+      // the busiest lane's
+      const int nj = __popc(todo0);
+      int inc = nj;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const int v = __shfl_up_sync(FULL, inc, d);
+        if (lane >= d) inc += v;
+      }
+      const int ntot = __shfl_sync(FULL, inc, 31);
+      int pos = inc - nj;
+      uint16_t* Lj = jlS[w];
       unsigned todo = todo0;
       while (todo) {
         const int bpos = __ffs(todo) - 1;
         todo &= todo - 1;
-        const int x = xl + (bpos & 7), d = bpos >> 3;
+        Lj[pos++] = (uint16_t)((xl + (bpos & 7)) | ((bpos >> 3) << 8));
+      }
+      __syncwarp();
+      for (int q = lane; q < ntot; q += 32) {
+        const int e = Lj[q];
+        const int x = e & 0xFF, d = e >> 8;
         const int xb = x + (d == 0 ? 0 : (d == 1 ? -1 : 1));
         const unsigned sa = ownS[w][x], sb = abS[w][8 + xb];
         const long long tb = xb < 0 ? ta - 1 : (xb >= TW ? ta + 1 : ta);
