@@ -1,6 +1,7 @@
 """CPU checks of bench.py's host logic: the reference arm's JSON line, the
-replica (N > 1) launch under torchrun with two gloo ranks, and the max over
-ranks used for the whole-job time."""
+replica (N > 1) launch under torchrun with two gloo ranks, the max over
+ranks used for the whole-job time, and the source hash that keeps a committed
+traffic figure to the code it was measured on."""
 import json
 import os
 import socket
@@ -80,3 +81,24 @@ def test_max_over_ranks_gloo():
         p.join(timeout=60)
         assert p.exitcode == 0
     assert res == {0: 2.5, 1: 2.5}
+
+
+def test_traffic_figure_only_for_the_sources_it_was_measured_on(tmp_path, monkeypatch):
+    """bench.py reports a committed ncu traffic figure only while the kernel
+    sources hash to the value recorded beside it; comments do not count."""
+    sys.path.insert(0, ROOT)
+    import bench
+    src = tmp_path / "connected_component_labelling_gb300" / "csrc"
+    src.mkdir(parents=True)
+    (src / "k.cuh").write_text("__global__ void k() { int a = 1; }  // first\n")
+    (tmp_path / "profiles").mkdir()
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    sha = bench.source_sha()
+    entry = {"source_sha": sha, "kernels": {"w": {"tile_local": 4.9}}}
+    (tmp_path / "profiles" / "traffic.json").write_text(json.dumps(entry))
+    assert bench.traffic_per_px("tile_local", "w") == 4.9
+    assert bench.traffic_per_px("number", "w") is None
+    (src / "k.cuh").write_text("__global__ void k() { int a = 1; }  /* changed comment */\n")
+    assert bench.source_sha() == sha and bench.traffic_per_px("tile_local", "w") == 4.9
+    (src / "k.cuh").write_text("__global__ void k() { int a = 2; }\n")
+    assert bench.source_sha() != sha and bench.traffic_per_px("tile_local", "w") is None
