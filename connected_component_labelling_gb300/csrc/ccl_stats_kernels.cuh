@@ -89,9 +89,10 @@ __device__ __forceinline__ void stats_add_global(ccl_region_stat* e, int area, i
 }
 
 // A block per strip of SSEG areas of 256 columns x SR rows, taken one area
-// after another.  Blocks are small (four warps) and strips short, so that
-// many strips are in flight on an SM: the kernel waits on its shared-memory
-// chains more than it issues.  A warp takes one row of the area at a time, a lane 8
+// after another.  Blocks are small (four warps), strips short and a run's
+// label is read back through L1 rather than kept in shared memory, so that
+// many strips are in flight on an SM (twelve): the kernel waits on its
+// shared-memory chains more than it issues.  A warp takes one row of the area at a time, a lane 8
 // consecutive labels (as in k_tile_local).  The row's runs of equal label
 // (run starts from equal-to-left masks) are listed in shared memory and dealt
 // out to the warp's lanes, a run each, so that busy rows keep every lane
@@ -200,7 +201,6 @@ __global__ void __launch_bounds__(STATS_NT, STATS_NT == 256 ? 6 : 12) k_region_s
                                                      ccl_region_stat* stats, long long capacity,
                                                      Geom g, int stripsX, int* status) {
   __shared__ StatsTable ta, ts;                               // the area's and the strip's tables
-  __shared__ __align__(16) int rowS[STATS_NWARPS][TW];        // the warp's row of labels
   __shared__ uint16_t runS[STATS_NWARPS][TW + 1];             // its runs' first columns
   // some partial went straight to a global entry (a crowded table): then a
   // label of the strip's table may have global partials too, so none of that
@@ -226,7 +226,6 @@ __global__ void __launch_bounds__(STATS_NT, STATS_NT == 256 ? 6 : 12) k_region_s
   const int32_t* li = labels + (long long)b * g.HW;
   const bool topIn = y0 > 0, botIn = y1 < g.H - 1;   // rows with neighbours outside
   const bool stripL = x0 > 0, stripR = (long long)x0 + sw < g.W;
-  int* rb = rowS[warp];
   uint16_t* L = runS[warp];
   const int nseg = (sw + TW - 1) / TW;
   for (int s = 0; s < nseg; ++s) {
@@ -252,9 +251,7 @@ __global__ void __launch_bounds__(STATS_NT, STATS_NT == 256 ? 6 : 12) k_region_s
 #pragma unroll
       for (int j = 1; j < PX; ++j) same |= (v[j] == v[j - 1] ? 1u : 0u) << j;
       unsigned starts = vmask & ~same;
-      // the row's labels and run starts in shared memory, the runs listed in order
-      *reinterpret_cast<int4*>(rb + xl) = make_int4(v[0], v[1], v[2], v[3]);
-      *reinterpret_cast<int4*>(rb + xl + 4) = make_int4(v[4], v[5], v[6], v[7]);
+      // the row's runs listed in order (a run's label is read back through L1)
       const int ns = __popc(starts);
       int inc = ns;
 #pragma unroll
@@ -273,7 +270,7 @@ __global__ void __launch_bounds__(STATS_NT, STATS_NT == 256 ? 6 : 12) k_region_s
       __syncwarp();
       const bool edgeRow = (y == y0 && topIn) || (y == y1 && botIn);
       for (int k = lane; k < nrun; k += 32) {
-        const int l = rb[L[k]];
+        const int l = __ldg(row - xl + L[k]);
         if (l == 0) continue;
         if (l < 0 || l > nb) {
           raise_flag(status, FLAG_BAD_LABEL);
